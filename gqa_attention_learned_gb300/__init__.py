@@ -1,0 +1,189 @@
+"""Python binding of libsinkattn (GQA attention with learned per-head sinks).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI declared in ``include/sinkattn.h``.  PyTorch supplies
+device memory and the current stream.  There is no fallback: if the shared
+library is missing or fails to load, every call raises.
+"""
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsinkattn.so")
+
+OK, INVALID_ARGUMENT, UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA_ERROR = range(5)
+
+_c_int, _c_float, _c_size, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_void_p
+
+# name -> (restype, argtypes), in the order of include/sinkattn.h
+SIGNATURES = {
+    "sinkattn_status_string": (ctypes.c_char_p, [_c_int]),
+    "sinkattn_version": (_c_int, []),
+    "sinkattn_decode_plan": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                      ctypes.POINTER(_c_int), ctypes.POINTER(_c_size)]),
+    "sinkattn_decode": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _vp, _c_float, _vp, _vp,
+                                 _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                 _vp, _c_size, _vp]),
+    "sinkattn_prefill": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _vp, _c_float, _vp,
+                                  _vp, _c_int, _c_int, _c_int, _vp]),
+    "sinkattn_prefill_paged": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _vp, _c_int,
+                                        _vp, _c_int, _c_int, _vp, _c_float, _vp, _vp, _c_int,
+                                        _c_int, _c_int, _c_int, _vp]),
+}
+
+_lib = None
+
+
+class SinkAttnError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn} failed: {status_string(status)} ({status})")
+
+
+def load():
+    """Load libsinkattn.so (built by ``build.build()``); raises if absent."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libsinkattn.so not built ({LIB_PATH}); run "
+                               "`python -m gqa_attention_learned_gb300.build`")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype, fn.argtypes = res, args
+        _lib = lib
+    return _lib
+
+
+def status_string(status):
+    return load().sinkattn_status_string(int(status)).decode()
+
+
+def _check(fn, status):
+    if status != OK:
+        raise SinkAttnError(fn, status)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _want(t, name, dtype, dims=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if dims is not None and t.dim() != dims:
+        raise ValueError(f"{name} must have {dims} dims, got shape {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def decode_plan(batch, num_qo_heads, num_kv_heads, max_kv_len, num_splits=0, num_sms=0,
+                head_dim=64, page_size=16):
+    """Split count and workspace bytes that `decode` will use (host only)."""
+    s = _c_int(num_splits)
+    w = _c_size(0)
+    _check("sinkattn_decode_plan",
+           load().sinkattn_decode_plan(batch, num_qo_heads, num_kv_heads, head_dim, page_size,
+                                       max_kv_len, num_sms, ctypes.byref(s), ctypes.byref(w)))
+    return s.value, w.value
+
+
+def decode(q, k_cache, v_cache, page_table, kv_lens, sinks, scale, max_kv_len, *, out=None,
+           lse=None, num_splits=0, workspace=None, stream=None, want_lse=True):
+    """Paged decode.  q [B, Hq, 64] bf16; caches [pages, Hkv, 16, 64] bf16;
+    page_table [B, max_pages] int32; kv_lens [B] int32; sinks [Hq] fp32.
+    Returns (out [B, Hq, 64] bf16, lse [B, Hq] fp32 or None)."""
+    dev = q.device
+    _want(q, "q", torch.bfloat16, 3)
+    _want(k_cache, "k_cache", torch.bfloat16, 4, dev)
+    _want(v_cache, "v_cache", torch.bfloat16, 4, dev)
+    _want(page_table, "page_table", torch.int32, 2, dev)
+    _want(kv_lens, "kv_lens", torch.int32, 1, dev)
+    _want(sinks, "sinks", torch.float32, 1, dev)
+    batch, hq, d = q.shape
+    num_pages, hkv, page, d2 = k_cache.shape
+    if v_cache.shape != k_cache.shape or d2 != d:
+        raise ValueError("k_cache/v_cache shapes disagree with q")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty(batch, hq, dtype=torch.float32, device=dev)
+    splits, ws_bytes = decode_plan(batch, hq, hkv, max_kv_len, num_splits, head_dim=d,
+                                   page_size=page) if batch else (1, 0)
+    if workspace is None and ws_bytes:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    with torch.cuda.device(dev):
+        _check("sinkattn_decode", load().sinkattn_decode(
+            _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table), page_table.shape[1],
+            _ptr(kv_lens), _ptr(sinks), float(scale), _ptr(out), _ptr(lse), batch, hq, hkv, d,
+            page, num_pages, int(max_kv_len), int(num_splits), _ptr(workspace), ws_len,
+            _stream(stream)))
+    return out, lse
+
+
+def prefill(q, k, v, cu_seqlens, sinks, scale, max_seqlen, *, out=None, lse=None, stream=None,
+            want_lse=True):
+    """Ragged causal prefill.  q [T, Hq, 64], k/v [T, Hkv, 64] bf16;
+    cu_seqlens [n+1] int32.  Returns (out [T, Hq, 64], lse [T, Hq] or None)."""
+    dev = q.device
+    _want(q, "q", torch.bfloat16, 3)
+    _want(k, "k", torch.bfloat16, 3, dev)
+    _want(v, "v", torch.bfloat16, 3, dev)
+    _want(cu_seqlens, "cu_seqlens", torch.int32, 1, dev)
+    _want(sinks, "sinks", torch.float32, 1, dev)
+    total, hq, d = q.shape
+    hkv = k.shape[1]
+    if k.shape != v.shape or k.shape[0] != total or k.shape[2] != d:
+        raise ValueError("q/k/v shapes disagree")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty(total, hq, dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        _check("sinkattn_prefill", load().sinkattn_prefill(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), cu_seqlens.numel() - 1, total,
+            int(max_seqlen), _ptr(sinks), float(scale), _ptr(out), _ptr(lse), hq, hkv, d,
+            _stream(stream)))
+    return out, lse
+
+
+def prefill_paged(q, cu_seqlens_q, k_cache, v_cache, page_table, kv_lens, sinks, scale,
+                  max_q_len, max_kv_len, *, out=None, lse=None, stream=None, want_lse=True):
+    """Chunked prefill against a paged KV prefix (bottom-right causal)."""
+    dev = q.device
+    _want(q, "q", torch.bfloat16, 3)
+    _want(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1, dev)
+    _want(k_cache, "k_cache", torch.bfloat16, 4, dev)
+    _want(v_cache, "v_cache", torch.bfloat16, 4, dev)
+    _want(page_table, "page_table", torch.int32, 2, dev)
+    _want(kv_lens, "kv_lens", torch.int32, 1, dev)
+    _want(sinks, "sinks", torch.float32, 1, dev)
+    total, hq, d = q.shape
+    num_pages, hkv, page, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty(total, hq, dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        _check("sinkattn_prefill_paged", load().sinkattn_prefill_paged(
+            _ptr(q), _ptr(cu_seqlens_q), cu_seqlens_q.numel() - 1, total, int(max_q_len),
+            _ptr(k_cache), _ptr(v_cache), _ptr(page_table), page_table.shape[1], _ptr(kv_lens),
+            num_pages, int(max_kv_len), _ptr(sinks), float(scale), _ptr(out), _ptr(lse), hq, hkv,
+            d, page, _stream(stream)))
+    return out, lse

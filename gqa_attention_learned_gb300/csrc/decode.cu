@@ -1,0 +1,396 @@
+// Paged-KV decode with learned sinks: split-KV kernel + log-sum-exp merge.
+//
+// Operation: "GPT-OSS on day 0" (Perplexity blog), section "Kernels for
+// GPT-OSS / Sink Attention" -- online softmax with the running max started at
+// the head's sink (scale d = 1) in the first KV block only, other blocks
+// started at -inf, blocks merged by log-sum-exp.
+//
+// Design (GB300, HBM-bound):
+//  * One CTA = one (request, KV head, 8-query-head block, KV chunk).  Its
+//    NW warps take the chunk's 16-token pages round-robin, each warp running
+//    its own STAGES-deep TMA pipeline: lane 0 issues two 3-D bulk tensor
+//    copies per page (K and V tile, 2 KB each, 128-byte swizzle) onto the
+//    stage's mbarrier.  No register staging, so many pages stay in flight.
+//  * The GQA group shares every K/V tile: S^T[16 tok x 8 heads] = K . Q^T and
+//    O^T[64 x 8] += V^T . P^T, each 4 mma.sync.m16n8k16 (bf16 in, fp32 acc).
+//    P^T goes from the score accumulator layout to the B-operand layout with
+//    movmatrix.trans; K and V^T come from shared memory by ldmatrix(.trans),
+//    bank-conflict free thanks to the swizzle.
+//  * Online softmax in base 2: scores scaled by scale*log2(e), sink by log2(e).
+//    Row max is reduced with 3 xor-shuffles per page; the running sum stays
+//    per lane and is reduced once at the end.
+//  * Warps of a CTA merge through shared memory.  A request with one chunk is
+//    finished in place; otherwise each chunk writes (o/d, lse) to the
+//    workspace and the merge kernel combines them.
+// There is no tensor-memory (tcgen05) path here: n = 8 query heads per KV
+// head is far below tcgen05's minimum tile, and the work is bound by HBM.
+
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+#include <cmath>
+
+namespace sa {
+namespace {
+
+constexpr int kNW = 4;          // warps per CTA
+constexpr int kStages = 4;      // pages in flight per warp
+constexpr int kTileBytes = kPageSize * kHeadDim * 2;   // 2048
+constexpr int kStageBytes = 2 * kTileBytes;            // K + V
+constexpr int kHeadsPerTile = 8;
+
+struct __align__(16) MergeSmem {
+  float o[kNW][kHeadsPerTile][kHeadDim];
+  float m[kNW][kHeadsPerTile];
+  float d[kNW][kHeadsPerTile];
+};
+
+constexpr int kPipeBytes = kNW * kStages * kStageBytes;
+constexpr int kBarOffset = kPipeBytes;
+constexpr int kSmemBytes = kBarOffset + kNW * kStages * 8 + 1024;  // + alignment slack
+static_assert(sizeof(MergeSmem) <= kPipeBytes, "merge scratch aliases the stages");
+
+__device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Chunk count of one request under the plan; 0 marks a request whose
+// arguments are out of range (its outputs become NaN).
+__device__ __forceinline__ int request_chunks(int kv_len, int max_pages_per_seq, int num_splits,
+                                              int pages_per_chunk) {
+  if (kv_len < 0) return 0;
+  const int npages = ceil_div(kv_len, kPageSize);
+  if (npages > max_pages_per_seq || npages > num_splits * pages_per_chunk) return 0;
+  return npages == 0 ? 1 : ceil_div(npages, pages_per_chunk);
+}
+
+__global__ void __launch_bounds__(kNW * 32)
+decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+              const DecodeParams p) {
+  const int chunk = blockIdx.x;
+  const int hb = blockIdx.y % p.head_blocks;
+  const int kvh = blockIdx.y / p.head_blocks;
+  const int b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+
+  const int kv_len = p.kv_lens[b];
+  const int nchunks = request_chunks(kv_len, p.max_pages_per_seq, p.num_splits, p.pages_per_chunk);
+  bool bad = nchunks == 0;
+  if (!bad && chunk >= nchunks) return;        // uniform over the CTA
+  if (bad && chunk != 0) return;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kBarOffset) + warp * kStages;
+  uint8_t *stages = smem + warp * kStages * kStageBytes;
+
+  const int head0 = kvh * p.group + hb * kHeadsPerTile;
+  const int nheads = min(kHeadsPerTile, p.group - hb * kHeadsPerTile);
+  const int npages = bad ? 0 : ceil_div(kv_len, kPageSize);
+  const int p_begin = chunk * p.pages_per_chunk;
+  const int p_end = min(npages, p_begin + p.pages_per_chunk);
+  const int first = p_begin + warp;
+  const int n_my = p_end > first ? ceil_div(p_end - first, kNW) : 0;
+  const int32_t *table = p.page_table + static_cast<size_t>(b) * p.max_pages_per_seq;
+
+  if (lane == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+    fence_mbar_init();
+    if (warp == 0) {
+      tma_prefetch_desc(&kmap);
+      tma_prefetch_desc(&vmap);
+    }
+  }
+  __syncwarp();
+
+  // Q^T as the B operand: lane (g, t) holds head g, dims 16ks+2t.. and 16ks+8+2t..
+  uint32_t qb[4][2];
+  {
+    const bool live = g < nheads;
+    const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+        p.q + (static_cast<size_t>(b) * p.num_qo_heads + head0 + (live ? g : 0)) * kHeadDim);
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      qb[ks][0] = live ? __ldg(qrow + 8 * ks + t) : 0u;
+      qb[ks][1] = live ? __ldg(qrow + 8 * ks + 4 + t) : 0u;
+    }
+  }
+
+  // Softmax state for heads 2t and 2t+1 (identical across the 8 g-lanes).
+  float m0 = -INFINITY, m1 = -INFINITY, d0 = 0.f, d1 = 0.f;
+  if (chunk == 0 && warp == 0) {
+    const float s0 = (2 * t < nheads) ? p.sinks[head0 + 2 * t] * kLog2e : -INFINITY;
+    const float s1 = (2 * t + 1 < nheads) ? p.sinks[head0 + 2 * t + 1] * kLog2e : -INFINITY;
+    m0 = s0;
+    m1 = s1;
+    if (g == 0) {            // the sink's e^(sink - m) = 1 counted once
+      d0 = 1.f;
+      d1 = 1.f;
+    }
+  }
+  float o[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+
+  // Page ids of this warp's pages, 32 at a time (lane j holds page j of the batch).
+  auto load_ids = [&](int base) -> int {
+    const int j = base + lane;
+    return j < n_my ? table[first + j * kNW] : -1;
+  };
+  int ids_cur = load_ids(0), ids_next = load_ids(32);
+  bool lane_bad = false;     // meaningful on lane 0
+
+  auto issue = [&](int j) {  // all lanes call; lane 0 issues
+    if ((j & 31) == 0 && j > 0) {
+      ids_cur = ids_next;
+      ids_next = load_ids(j + 32);
+    }
+    const int pid = __shfl_sync(0xffffffffu, ids_cur, j & 31);
+    if (lane == 0) {
+      uint64_t *bar = &bars[j % kStages];
+      uint8_t *dst = stages + (j % kStages) * kStageBytes;
+      if (pid >= 0 && pid < p.num_pages) {
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(bar, kStageBytes);
+        tma_load_3d(dst, &kmap, bar, 0, kvh * kPageSize, pid);
+        tma_load_3d(dst + kTileBytes, &vmap, bar, 0, kvh * kPageSize, pid);
+      } else {
+        lane_bad = true;     // skip the copy; the phase still completes
+        mbar_arrive(bar);
+      }
+    }
+  };
+
+  const int n_pro = min(kStages, n_my);
+  for (int j = 0; j < n_pro; ++j) issue(j);
+
+  // ldmatrix lane roles (see header comment): K tiles non-transposed, V transposed.
+  const int k_row = (lane & 7) + 8 * ((lane >> 3) & 1);
+  const int k_hi = lane >> 4;
+  const int v_row = (lane & 7) + 8 * (lane >> 4);
+  const int v_hi = (lane >> 3) & 1;
+
+  for (int i = 0; i < n_my; ++i) {
+    const int st = i % kStages;
+    if (!mbar_wait(&bars[st], (i / kStages) & 1)) {
+      // A copy never landed: report, then drain (bounded) whatever else this
+      // warp still has in flight before the stages are reused below.
+      lane_bad = true;
+      bad = true;
+      for (int j = i + 1; j < min(n_my, i + kStages); ++j)
+        mbar_wait(&bars[j % kStages], (j / kStages) & 1);
+      break;
+    }
+    const uint32_t kbase = smem_u32(stages + st * kStageBytes);
+    const uint32_t vbase = kbase + kTileBytes;
+
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      uint32_t a[4];
+      const int c = 2 * ks + k_hi;
+      ldsm_x4(kbase + k_row * 128 + ((c ^ (k_row & 7)) << 4), a);
+      mma_bf16_16816(s, a, qb[ks][0], qb[ks][1]);
+    }
+
+    const int tok0 = (first + i * kNW) * kPageSize;
+    const bool partial = tok0 + kPageSize > kv_len;
+    // s[0]: token g / head 2t, s[1]: token g / head 2t+1, s[2], s[3]: token g+8.
+#pragma unroll
+    for (int r = 0; r < 4; ++r) s[r] *= p.scale_log2;
+    if (partial) {
+      if (tok0 + g >= kv_len) s[0] = s[1] = -INFINITY;
+      if (tok0 + g + 8 >= kv_len) s[2] = s[3] = -INFINITY;
+    }
+    float x0 = fmaxf(s[0], s[2]), x1 = fmaxf(s[1], s[3]);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
+      x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
+    }
+    const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+    const float u0 = n0 == -INFINITY ? 0.f : n0;
+    const float u1 = n1 == -INFINITY ? 0.f : n1;
+    const float a0 = ex2(m0 - u0), a1 = ex2(m1 - u1);
+    const float p0 = ex2(s[0] - u0), p1 = ex2(s[1] - u1);
+    const float p2 = ex2(s[2] - u0), p3 = ex2(s[3] - u1);
+    d0 = d0 * a0 + p0 + p2;
+    d1 = d1 * a1 + p1 + p3;
+    m0 = n0;
+    m1 = n1;
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+      o[mt][0] *= a0;
+      o[mt][1] *= a1;
+      o[mt][2] *= a0;
+      o[mt][3] *= a1;
+    }
+    const uint32_t pb0 = movmatrix_trans(pack_bf16(p0, p1));   // tokens 0..7
+    const uint32_t pb1 = movmatrix_trans(pack_bf16(p2, p3));   // tokens 8..15
+
+    uint32_t keep01 = 0xffffffffu, keep23 = 0xffffffffu;
+    if (partial) {
+      keep01 = (tok0 + 2 * t < kv_len ? 0x0000ffffu : 0u) |
+               (tok0 + 2 * t + 1 < kv_len ? 0xffff0000u : 0u);
+      keep23 = (tok0 + 2 * t + 8 < kv_len ? 0x0000ffffu : 0u) |
+               (tok0 + 2 * t + 9 < kv_len ? 0xffff0000u : 0u);
+    }
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+      uint32_t a[4];
+      const int c = 2 * mt + v_hi;
+      ldsm_x4_trans(vbase + v_row * 128 + ((c ^ (v_row & 7)) << 4), a);
+      a[0] &= keep01;       // padded slots may hold anything (even NaN)
+      a[1] &= keep01;
+      a[2] &= keep23;
+      a[3] &= keep23;
+      mma_bf16_16816(o[mt], a, pb0, pb1);
+    }
+    __syncwarp();
+    const int j = i + kStages;
+    if (j < n_my) issue(j);
+  }
+
+  // Full per-head sums.
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    d0 += __shfl_xor_sync(0xffffffffu, d0, off);
+    d1 += __shfl_xor_sync(0xffffffffu, d1, off);
+  }
+  bad = bad || (__shfl_sync(0xffffffffu, lane_bad ? 1 : 0, 0) != 0);
+
+  __syncthreads();   // every warp is done with its stages: alias them
+  MergeSmem &ms = *reinterpret_cast<MergeSmem *>(smem);
+  __shared__ int cta_bad;
+  if (threadIdx.x == 0) cta_bad = 0;
+  if (g == 0) {
+    ms.m[warp][2 * t] = m0;
+    ms.m[warp][2 * t + 1] = m1;
+    ms.d[warp][2 * t] = d0;
+    ms.d[warp][2 * t + 1] = d1;
+  }
+#pragma unroll
+  for (int mt = 0; mt < 4; ++mt) {
+    ms.o[warp][2 * t][16 * mt + g] = o[mt][0];
+    ms.o[warp][2 * t + 1][16 * mt + g] = o[mt][1];
+    ms.o[warp][2 * t][16 * mt + 8 + g] = o[mt][2];
+    ms.o[warp][2 * t + 1][16 * mt + 8 + g] = o[mt][3];
+  }
+  __syncthreads();
+  if (bad) atomicOr(&cta_bad, 1);
+  __syncthreads();
+  const bool failed = cta_bad != 0;
+
+  for (int item = threadIdx.x; item < kHeadsPerTile * (kHeadDim / 4); item += kNW * 32) {
+    const int hh = item / (kHeadDim / 4);
+    const int dq = (item % (kHeadDim / 4)) * 4;
+    if (hh >= nheads) continue;
+    float mx = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kNW; ++w) mx = fmaxf(mx, ms.m[w][hh]);
+    float den = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int w = 0; w < kNW; ++w) {
+      const float mw = ms.m[w][hh];
+      const float wt = mw == -INFINITY ? 0.f : ex2(mw - mx);
+      den += wt * ms.d[w][hh];
+      const float4 ov = *reinterpret_cast<const float4 *>(&ms.o[w][hh][dq]);
+      acc[0] += wt * ov.x;
+      acc[1] += wt * ov.y;
+      acc[2] += wt * ov.z;
+      acc[3] += wt * ov.w;
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    float lse2 = den > 0.f ? mx + lg2(den) : -INFINITY;
+    if (failed) {
+      acc[0] = acc[1] = acc[2] = acc[3] = NAN;
+      lse2 = NAN;
+    }
+    const int h = head0 + hh;
+    const size_t row = static_cast<size_t>(b) * p.num_qo_heads + h;
+    if (nchunks <= 1) {
+      uint2 packed;
+      packed.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+      packed.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+      *reinterpret_cast<uint2 *>(p.out + row * kHeadDim + dq) = packed;
+      if (dq == 0 && p.lse) p.lse[row] = lse2 * kLn2;
+    } else {
+      const size_t wrow = static_cast<size_t>(chunk) * p.batch * p.num_qo_heads + row;
+      *reinterpret_cast<float4 *>(p.ws_o + wrow * kHeadDim + dq) =
+          make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+      if (dq == 0) p.ws_lse[wrow] = lse2;
+    }
+  }
+}
+
+// One warp per (request, query head): log-sum-exp merge of the chunk results.
+__global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
+  const int warp_global = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (warp_global >= p.batch * p.num_qo_heads) return;
+  const int b = warp_global / p.num_qo_heads;
+  const int nchunks =
+      request_chunks(p.kv_lens[b], p.max_pages_per_seq, p.num_splits, p.pages_per_chunk);
+  if (nchunks <= 1) return;     // finished (or failed) inside the decode kernel
+  const size_t row = warp_global;
+  const size_t stride = static_cast<size_t>(p.batch) * p.num_qo_heads;
+
+  float l[8];
+  float mx = -INFINITY;
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    const int c = lane + 32 * r;
+    l[r] = c < nchunks ? p.ws_lse[c * stride + row] : -INFINITY;
+    mx = fmaxf(mx, l[r]);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  float wsum = 0.f;
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    l[r] = (l[r] == -INFINITY) ? 0.f : ex2(l[r] - mx);   // weight of chunk
+    wsum += l[r];
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
+
+  float2 acc = make_float2(0.f, 0.f);
+  for (int c = 0; c < nchunks; ++c) {
+    float w = 0.f;
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+      if ((c >> 5) == r) w = __shfl_sync(0xffffffffu, l[r], c & 31);
+    if (w != 0.f) {
+      const float2 v = *reinterpret_cast<const float2 *>(p.ws_o + (c * stride + row) * kHeadDim +
+                                                         2 * lane);
+      acc.x += w * v.x;
+      acc.y += w * v.y;
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  reinterpret_cast<uint32_t *>(p.out + row * kHeadDim)[lane] = pack_bf16(acc.x * inv, acc.y * inv);
+  if (lane == 0 && p.lse) p.lse[row] = (wsum > 0.f ? mx + lg2(wsum) : -INFINITY) * kLn2;
+}
+
+}  // namespace
+
+int decode_ctas_per_sm() { return 3; }
+
+int decode_max_splits() { return 256; }  // merge_kernel holds 8 x 32 chunk weights
+
+cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParams &p,
+                          cudaStream_t stream) {
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  cudaError_t err = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemBytes);
+  if (err != cudaSuccess) return err;
+  dim3 grid(p.num_splits, p.num_kv_heads * p.head_blocks, p.batch);
+  decode_kernel<<<grid, kNW * 32, kSmemBytes, stream>>>(kmap, vmap, p);
+  err = cudaGetLastError();
+  if (err != cudaSuccess || p.num_splits <= 1) return err;
+  const int warps = p.batch * p.num_qo_heads;
+  merge_kernel<<<(warps + 7) / 8, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace sa

@@ -1,0 +1,63 @@
+// Internal interface between the C ABI layer (sinkattn_api.cu) and the
+// kernel translation units.  Not installed; no torch types anywhere.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace sa {
+
+constexpr int kHeadDim = 64;
+constexpr int kPageSize = 16;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// ----------------------------------------------------------------- decode
+struct DecodeParams {
+  const uint16_t *q;            // bf16 [B][Hq][64]
+  const int32_t *page_table;    // [B][max_pages_per_seq]
+  const int32_t *kv_lens;       // [B]
+  const float *sinks;           // [Hq]
+  uint16_t *out;                // bf16 [B][Hq][64]
+  float *lse;                   // [B][Hq] or null
+  float *ws_o;                  // fp32 [splits][B][Hq][64] (splits > 1)
+  float *ws_lse;                // fp32 [splits][B][Hq]     (base-2 lse)
+  float scale_log2;             // scale * log2(e)
+  int max_pages_per_seq;
+  int batch, num_qo_heads, num_kv_heads, group, head_blocks;
+  int num_pages, num_splits, pages_per_chunk;
+};
+
+// Number of CTAs the decode kernel may keep resident per SM (for planning).
+int decode_ctas_per_sm();
+// Largest split count the merge kernel handles.
+int decode_max_splits();
+
+cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap,
+                          const DecodeParams &p, cudaStream_t stream);
+
+// ---------------------------------------------------------------- prefill
+struct PrefillParams {
+  const uint16_t *q;             // bf16 [Tq][Hq][64]
+  const int32_t *cu_seqlens_q;   // [n+1]
+  const int32_t *cu_seqlens_k;   // [n+1] (contiguous K/V) or null (paged)
+  const int32_t *page_table;     // paged K/V: [n][max_pages_per_seq]
+  const int32_t *kv_lens;        // paged K/V: [n]
+  const float *sinks;            // [Hq]
+  uint16_t *out;                 // bf16 [Tq][Hq][64]
+  float *lse;                    // [Tq][Hq] or null
+  float scale_log2;
+  int num_seqs, total_q, total_k, max_q_len, max_kv_len;
+  int num_qo_heads, num_kv_heads, group;
+  int max_pages_per_seq, num_pages;
+  int paged;                     // 0: k/v [Tk][Hkv][64], 1: paged cache
+  int num_q_tiles;               // ceil(max_q_len / tile)
+};
+
+cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap,
+                           const CUtensorMap &vmap, const PrefillParams &p,
+                           cudaStream_t stream);
+
+}  // namespace sa

@@ -1,0 +1,231 @@
+// C ABI of libsinkattn: argument checks, split planning, TMA descriptor
+// encoding and kernel launches.  The operations are specified in
+// include/sinkattn.h.  Nothing here allocates device memory or synchronises.
+
+#include "sinkattn.h"
+#include "kernels.cuh"
+
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <mutex>
+
+namespace {
+
+using sa::kHeadDim;
+using sa::kPageSize;
+
+constexpr int kMaxDevices = 64;
+constexpr int kMinPagesPerChunk = 16;   // keeps merge traffic under ~3% of KV
+constexpr int kWavesTarget = 4;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+int device_sm_count() {
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < kMaxDevices) {
+    const int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < kMaxDevices) cache[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+// bf16 tensor viewed as [outer][rows][64] with 128-byte rows; box = box_rows
+// rows of one outer index, 128-byte swizzle.
+bool encode_rows_map(CUtensorMap *map, const void *base, unsigned long long rows_per_outer,
+                     unsigned long long outer, unsigned box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), rows_per_outer, outer};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim * 2),
+                           static_cast<cuuint64_t>(rows_per_outer * kHeadDim * 2)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim), box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+struct DecodePlan {
+  int num_splits = 1;
+  int pages_per_chunk = 1;
+  size_t workspace_bytes = 0;
+};
+
+DecodePlan plan_decode(int batch, int num_qo_heads, int num_kv_heads, int max_kv_len, int num_sms,
+                       int requested) {
+  DecodePlan plan;
+  const int group = num_qo_heads / num_kv_heads;
+  const int head_blocks = ceil_div(group, 8);
+  const int max_pages = std::max(1, ceil_div(max_kv_len, kPageSize));
+  int s;
+  if (requested > 0) {
+    s = requested;
+  } else {
+    const long long units = static_cast<long long>(batch) * num_kv_heads * head_blocks;
+    const long long slots = static_cast<long long>(std::max(num_sms, 1)) * sa::decode_ctas_per_sm();
+    s = static_cast<int>(std::min<long long>((kWavesTarget * slots + units - 1) / units, 1 << 20));
+    s = std::min(s, std::max(1, max_pages / kMinPagesPerChunk));
+  }
+  s = std::max(1, std::min({s, sa::decode_max_splits(), max_pages}));
+  plan.pages_per_chunk = ceil_div(max_pages, s);
+  plan.num_splits = ceil_div(max_pages, plan.pages_per_chunk);
+  if (plan.num_splits > 1) {
+    const size_t rows = static_cast<size_t>(plan.num_splits) * batch * num_qo_heads;
+    plan.workspace_bytes = rows * kHeadDim * sizeof(float) + ((rows * sizeof(float) + 255) & ~size_t(255));
+  }
+  return plan;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *sinkattn_status_string(int status) {
+  switch (status) {
+    case SINKATTN_OK: return "ok";
+    case SINKATTN_INVALID_ARGUMENT: return "invalid argument";
+    case SINKATTN_UNSUPPORTED: return "unsupported configuration";
+    case SINKATTN_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case SINKATTN_CUDA_ERROR: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+int sinkattn_version(void) { return 100; }
+
+int sinkattn_decode_plan(int batch, int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
+                         int max_kv_len, int num_sms, int *num_splits, size_t *workspace_bytes) {
+  if (!num_splits || !workspace_bytes) return SINKATTN_INVALID_ARGUMENT;
+  if (head_dim != kHeadDim || page_size != kPageSize) return SINKATTN_UNSUPPORTED;
+  if (batch < 0 || num_qo_heads <= 0 || num_kv_heads <= 0 || max_kv_len < 0 || *num_splits < 0 ||
+      num_sms < 0 || num_qo_heads % num_kv_heads)
+    return SINKATTN_INVALID_ARGUMENT;
+  if (num_sms == 0) {
+    num_sms = device_sm_count();
+    if (num_sms == 0) return SINKATTN_CUDA_ERROR;
+  }
+  const DecodePlan plan = plan_decode(batch, num_qo_heads, num_kv_heads, max_kv_len, num_sms, *num_splits);
+  *num_splits = plan.num_splits;
+  *workspace_bytes = plan.workspace_bytes;
+  return SINKATTN_OK;
+}
+
+int sinkattn_decode(const void *q, const void *k_cache, const void *v_cache,
+                    const int32_t *page_table, int max_pages_per_seq, const int32_t *kv_lens,
+                    const float *sinks, float scale, void *out, float *lse, int batch,
+                    int num_qo_heads, int num_kv_heads, int head_dim, int page_size, int num_pages,
+                    int max_kv_len, int num_splits, void *workspace, size_t workspace_bytes,
+                    void *stream) {
+  if (head_dim != kHeadDim || page_size != kPageSize) return SINKATTN_UNSUPPORTED;
+  if (batch < 0 || num_qo_heads <= 0 || num_kv_heads <= 0 || num_qo_heads % num_kv_heads ||
+      max_kv_len < 0 || num_splits < 0 || num_pages <= 0 || max_pages_per_seq <= 0 ||
+      !std::isfinite(scale))
+    return SINKATTN_INVALID_ARGUMENT;
+  if (batch == 0) return SINKATTN_OK;
+  if (!q || !k_cache || !v_cache || !page_table || !kv_lens || !sinks || !out)
+    return SINKATTN_INVALID_ARGUMENT;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(page_table, 4) || !aligned(kv_lens, 4) || !aligned(sinks, 4) ||
+      (lse && !aligned(lse, 4)))
+    return SINKATTN_INVALID_ARGUMENT;
+  const int group = num_qo_heads / num_kv_heads;
+  const int head_blocks = ceil_div(group, 8);
+  if (batch > 65535 || static_cast<long long>(num_kv_heads) * head_blocks > 65535)
+    return SINKATTN_UNSUPPORTED;
+
+  const int sms = device_sm_count();
+  if (sms == 0) return SINKATTN_CUDA_ERROR;
+  const DecodePlan plan = plan_decode(batch, num_qo_heads, num_kv_heads, max_kv_len, sms, num_splits);
+  if (plan.num_splits > 1) {
+    if (!workspace || workspace_bytes < plan.workspace_bytes) return SINKATTN_WORKSPACE_TOO_SMALL;
+    if (!aligned(workspace, 16)) return SINKATTN_INVALID_ARGUMENT;
+  }
+
+  CUtensorMap kmap, vmap;
+  const unsigned long long rows = static_cast<unsigned long long>(num_kv_heads) * kPageSize;
+  if (!encode_rows_map(&kmap, k_cache, rows, num_pages, kPageSize) ||
+      !encode_rows_map(&vmap, v_cache, rows, num_pages, kPageSize))
+    return SINKATTN_CUDA_ERROR;
+
+  sa::DecodeParams p{};
+  p.q = static_cast<const uint16_t *>(q);
+  p.page_table = page_table;
+  p.kv_lens = kv_lens;
+  p.sinks = sinks;
+  p.out = static_cast<uint16_t *>(out);
+  p.lse = lse;
+  if (plan.num_splits > 1) {
+    p.ws_o = static_cast<float *>(workspace);
+    p.ws_lse = p.ws_o + static_cast<size_t>(plan.num_splits) * batch * num_qo_heads * kHeadDim;
+  }
+  p.scale_log2 = scale * sa::kLog2e;
+  p.max_pages_per_seq = max_pages_per_seq;
+  p.batch = batch;
+  p.num_qo_heads = num_qo_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = group;
+  p.head_blocks = head_blocks;
+  p.num_pages = num_pages;
+  p.num_splits = plan.num_splits;
+  p.pages_per_chunk = plan.pages_per_chunk;
+  cudaError_t err = sa::launch_decode(kmap, vmap, p, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? SINKATTN_OK : SINKATTN_CUDA_ERROR;
+}
+
+int sinkattn_prefill(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
+                     int num_seqs, int total_tokens, int max_seqlen, const float *sinks,
+                     float scale, void *out, float *lse, int num_qo_heads, int num_kv_heads,
+                     int head_dim, void *stream) {
+  if (head_dim != kHeadDim) return SINKATTN_UNSUPPORTED;
+  if (num_seqs < 0 || total_tokens < 0 || max_seqlen < 0 || num_qo_heads <= 0 ||
+      num_kv_heads <= 0 || num_qo_heads % num_kv_heads || !std::isfinite(scale))
+    return SINKATTN_INVALID_ARGUMENT;
+  if (num_seqs == 0 || total_tokens == 0) return SINKATTN_OK;
+  if (!q || !k || !v || !cu_seqlens || !sinks || !out) return SINKATTN_INVALID_ARGUMENT;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(cu_seqlens, 4) || !aligned(sinks, 4) || (lse && !aligned(lse, 4)))
+    return SINKATTN_INVALID_ARGUMENT;
+  (void)stream;
+  return SINKATTN_UNSUPPORTED;
+}
+
+int sinkattn_prefill_paged(const void *q, const int32_t *cu_seqlens_q, int num_seqs, int total_q,
+                           int max_q_len, const void *k_cache, const void *v_cache,
+                           const int32_t *page_table, int max_pages_per_seq,
+                           const int32_t *kv_lens, int num_pages, int max_kv_len,
+                           const float *sinks, float scale, void *out, float *lse,
+                           int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
+                           void *stream) {
+  (void)q; (void)cu_seqlens_q; (void)num_seqs; (void)total_q; (void)max_q_len; (void)k_cache;
+  (void)v_cache; (void)page_table; (void)max_pages_per_seq; (void)kv_lens; (void)num_pages;
+  (void)max_kv_len; (void)sinks; (void)scale; (void)out; (void)lse; (void)num_qo_heads;
+  (void)num_kv_heads; (void)head_dim; (void)page_size; (void)stream;
+  return SINKATTN_UNSUPPORTED;
+}
+
+}  // extern "C"

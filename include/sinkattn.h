@@ -1,0 +1,160 @@
+/*
+ * sinkattn.h -- C ABI of libsinkattn: GQA attention with a learned sink logit
+ * per query head, for NVIDIA GB300 (sm_103a).
+ *
+ * The operation ("GPT-OSS on day 0", Perplexity blog, section "Kernels for
+ * GPT-OSS / Sink Attention"; the page's displayed formulas were lost, this is
+ * the plainest reading of the surviving text): for query head h with KV head
+ * g(h) = h / (num_qo_heads / num_kv_heads) and the keys j it may see,
+ *
+ *     s_j   = scale * dot(q_h, k_{g(h),j})           (the sink is not scaled)
+ *     M     = max(sink_h, max_j s_j)
+ *     Z     = exp(sink_h - M) + sum_j exp(s_j - M)
+ *     out_h = sum_j exp(s_j - M) * v_{g(h),j} / Z     (the sink has no value row)
+ *     lse_h = M + ln Z                                (natural log, sink included)
+ *
+ * A row that sees no key gets out = 0, lse = sink.  sink = -inf is ordinary
+ * softmax attention; sink = +inf or NaN is undefined (the output is NaN).
+ * Work is split along the KV length the way the same section describes: the
+ * online softmax of the first KV block starts at max = sink, scale = 1; the
+ * other blocks start at max = -inf; blocks are merged by log-sum-exp.
+ *
+ * Conventions shared by every entry point
+ *   - bf16 = IEEE bfloat16 stored as uint16; all tensors are dense, row-major,
+ *     in device memory, 16-byte aligned, and owned by the caller.
+ *   - head_dim must be 64 and page_size 16 (else SINKATTN_UNSUPPORTED).
+ *   - num_qo_heads % num_kv_heads == 0; the GQA group is contiguous.
+ *   - Paged KV cache ("Accelerating Sonar through speculation", Perplexity
+ *     blog, section "Inference with speculative decoding": KV pages are
+ *     reserved per request and addressed through per-request page lists):
+ *       k_cache, v_cache : bf16 [num_pages][num_kv_heads][page_size][head_dim]
+ *       page_table       : int32 [batch][max_pages_per_seq]; token t of
+ *                          request b is slot t % page_size of page
+ *                          page_table[b][t / page_size].
+ *     Only the first ceil(kv_len / page_size) entries of a row are read.  A
+ *     page id outside [0, num_pages), kv_len < 0, or a kv_len that does not fit
+ *     the row or the declared maximum makes that request's outputs NaN; no
+ *     memory outside the given buffers is touched.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream), never synchronises, allocates nothing, and keeps no
+ *     state beyond a per-device cache of the SM count.  Calls are thread-safe.
+ *   - Return value: a sinkattn_status.  Argument checks happen on the host
+ *     before any launch; SINKATTN_CUDA_ERROR reports a launch failure.
+ */
+#ifndef SINKATTN_H
+#define SINKATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SINKATTN_API __attribute__((visibility("default")))
+#else
+#define SINKATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum sinkattn_status {
+  SINKATTN_OK = 0,
+  SINKATTN_INVALID_ARGUMENT = 1,   /* null/misaligned pointer, bad size */
+  SINKATTN_UNSUPPORTED = 2,        /* head_dim != 64, page_size != 16, ... */
+  SINKATTN_WORKSPACE_TOO_SMALL = 3,
+  SINKATTN_CUDA_ERROR = 4
+} sinkattn_status;
+
+/* Static description of a status code. */
+SINKATTN_API const char *sinkattn_status_string(int status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+SINKATTN_API int sinkattn_version(void);
+
+/*
+ * Split plan for sinkattn_decode (host only, no launch).
+ *   num_sms          : SMs to plan for; 0 = ask the current CUDA device.
+ *   num_splits       : in = requested split count (0 = choose), out = the
+ *                      split count sinkattn_decode will use.
+ *   workspace_bytes  : out = bytes of workspace that decode needs (0 when the
+ *                      plan has a single split).
+ * Same inputs give the same plan, so the plan can be made once and reused
+ * (e.g. under CUDA graph capture); max_kv_len is a host-side bound, so no
+ * device-to-host read is needed.
+ */
+SINKATTN_API int sinkattn_decode_plan(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                         int page_size, int max_kv_len, int num_sms,
+                         int *num_splits, size_t *workspace_bytes);
+
+/*
+ * Decode: one new query token per request against its paged KV.
+ *   q          : bf16 [batch][num_qo_heads][head_dim]
+ *   k_cache,
+ *   v_cache    : bf16 paged cache (see conventions), num_pages pages
+ *   page_table : int32 [batch][max_pages_per_seq]
+ *   kv_lens    : int32 [batch], keys per request (0 allowed)
+ *   sinks      : fp32 [num_qo_heads], in natural-log logit units
+ *   scale      : softmax scale applied to q.k
+ *   out        : bf16 [batch][num_qo_heads][head_dim]
+ *   lse        : fp32 [batch][num_qo_heads] (natural log, sink included);
+ *                may be NULL
+ *   max_kv_len : host-side upper bound on kv_lens (drives the split plan)
+ *   num_splits : 0 = choose (see sinkattn_decode_plan), else the split count
+ *   workspace  : device scratch of workspace_bytes (>= the plan's figure);
+ *                may be NULL when the plan has a single split.  Its contents
+ *                need no initialisation and are dead after the call.
+ * Long contexts run as num_splits KV chunks per (request, KV head) followed by
+ * a log-sum-exp merge kernel, the sink entering chunk 0 only.
+ */
+SINKATTN_API int sinkattn_decode(const void *q, const void *k_cache, const void *v_cache,
+                    const int32_t *page_table, int max_pages_per_seq,
+                    const int32_t *kv_lens, const float *sinks, float scale,
+                    void *out, float *lse,
+                    int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                    int page_size, int num_pages, int max_kv_len, int num_splits,
+                    void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Causal prefill over ragged sequences packed along the token axis.
+ *   q          : bf16 [total_tokens][num_qo_heads][head_dim]
+ *   k, v       : bf16 [total_tokens][num_kv_heads][head_dim]
+ *   cu_seqlens : int32 [num_seqs + 1], prefix sums of sequence lengths,
+ *                cu_seqlens[num_seqs] == total_tokens
+ *   max_seqlen : host-side upper bound on any sequence length
+ *   out        : bf16 [total_tokens][num_qo_heads][head_dim]
+ *   lse        : fp32 [total_tokens][num_qo_heads]; may be NULL
+ * Query i of a sequence sees keys 0..i of the same sequence.  A sequence
+ * longer than max_seqlen, or cu_seqlens that are not non-decreasing within
+ * [0, total_tokens], gives NaN rows for the offending sequence.
+ */
+SINKATTN_API int sinkattn_prefill(const void *q, const void *k, const void *v,
+                     const int32_t *cu_seqlens, int num_seqs, int total_tokens,
+                     int max_seqlen, const float *sinks, float scale,
+                     void *out, float *lse,
+                     int num_qo_heads, int num_kv_heads, int head_dim, void *stream);
+
+/*
+ * Chunked prefill ("extend"): new query tokens appended to a paged KV prefix.
+ * Request r owns queries cu_seqlens_q[r] .. cu_seqlens_q[r+1]-1 and kv_lens[r]
+ * keys in the paged cache; its last q_len keys are its own new tokens (already
+ * written to the cache).  Query i (0-based within the request) sees keys
+ * j <= kv_len - q_len + i (causal, aligned at the end).
+ *   q          : bf16 [total_q][num_qo_heads][head_dim]
+ *   out, lse   : as for prefill, [total_q]-major
+ *   max_q_len, max_kv_len : host-side bounds
+ * q_len > kv_len, or any bound exceeded, gives NaN rows for that request.
+ */
+SINKATTN_API int sinkattn_prefill_paged(const void *q, const int32_t *cu_seqlens_q, int num_seqs,
+                           int total_q, int max_q_len,
+                           const void *k_cache, const void *v_cache,
+                           const int32_t *page_table, int max_pages_per_seq,
+                           const int32_t *kv_lens, int num_pages, int max_kv_len,
+                           const float *sinks, float scale, void *out, float *lse,
+                           int num_qo_heads, int num_kv_heads, int head_dim,
+                           int page_size, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SINKATTN_H */

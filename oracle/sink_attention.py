@@ -101,10 +101,10 @@ def sink_attention(q, k, v, sink, scale, n_visible):
 def gather_paged_kv(cache, page_table, kv_len, kv_head, page_size):
     """Rows 0..kv_len-1 of one request's K (or V) for one KV head.
 
-    cache: [num_pages, Hkv, page_size, D]; token t lives in page
+    cache: [num_pages, Hkv, page_size, D], anything indexable that returns
+    values convertible to float64; token t lives in page
     page_table[t // page_size], slot t % page_size.
     """
-    cache = np.asarray(cache)
     t = np.arange(kv_len)
     pages = np.asarray(page_table)[t // page_size]
     return _f64(cache[pages, kv_head, t % page_size])

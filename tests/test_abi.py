@@ -1,0 +1,116 @@
+"""The C ABI library loads, exports every declared entry point, and rejects
+bad arguments on the host before touching a GPU (no compute calls here)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import gqa_attention_learned_gb300 as sa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sinkattn.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return re.findall(r"SINKATTN_API\s+[^;(]*?\b(sinkattn_\w+)\s*\(", text)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(sa.LIB_PATH):
+        from gqa_attention_learned_gb300 import build
+        build.build()
+    return sa.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_symbols()
+    assert len(names) >= 6
+    for name in names:
+        assert hasattr(lib, name), name
+        assert name in sa.SIGNATURES, f"binding lacks {name}"
+
+
+def test_status_strings(lib):
+    assert sa.status_string(0) == "ok"
+    assert "workspace" in sa.status_string(3)
+    assert sa.status_string(99) == "unknown status"
+    assert lib.sinkattn_version() >= 100
+
+
+def test_plan_is_host_only_and_deterministic(lib):
+    a = sa.decode_plan(64, 64, 8, 4096, num_sms=152)
+    b = sa.decode_plan(64, 64, 8, 4096, num_sms=152)
+    assert a == b
+    splits, ws = a
+    assert splits >= 1
+    assert (ws == 0) == (splits == 1)
+    # explicit split counts are honoured up to the page count
+    s, ws = sa.decode_plan(8, 64, 8, 131072, num_splits=8, num_sms=152)
+    assert s == 8 and ws == 8 * 8 * 64 * 65 * 4
+    s, _ = sa.decode_plan(1, 4, 1, 37, num_splits=64, num_sms=152)
+    assert s == 3      # 37 tokens = 3 pages: at most one page per split
+    s, ws = sa.decode_plan(4, 4, 1, 0, num_sms=152)
+    assert s == 1 and ws == 0
+
+
+def test_plan_long_context_splits(lib):
+    s, _ = sa.decode_plan(8, 64, 8, 131072, num_sms=152)
+    assert 8 <= s <= 256
+
+
+def test_plan_rejects_bad_arguments(lib):
+    with pytest.raises(sa.SinkAttnError) as e:
+        sa.decode_plan(1, 64, 8, 100, head_dim=128, num_sms=1)
+    assert e.value.status == sa.UNSUPPORTED
+    with pytest.raises(sa.SinkAttnError) as e:
+        sa.decode_plan(1, 64, 8, 100, page_size=32, num_sms=1)
+    assert e.value.status == sa.UNSUPPORTED
+    with pytest.raises(sa.SinkAttnError) as e:
+        sa.decode_plan(1, 60, 8, 100, num_sms=1)
+    assert e.value.status == sa.INVALID_ARGUMENT
+    with pytest.raises(sa.SinkAttnError) as e:
+        sa.decode_plan(-1, 64, 8, 100, num_sms=1)
+    assert e.value.status == sa.INVALID_ARGUMENT
+
+
+def _raw_decode(lib, **kw):
+    args = dict(q=None, k=None, v=None, table=None, maxp=1, lens=None, sinks=None, scale=0.125,
+                out=None, lse=None, batch=1, hq=8, hkv=1, d=64, page=16, pages=1, maxkv=16,
+                splits=0, ws=None, wsb=0, stream=None)
+    args.update(kw)
+    return lib.sinkattn_decode(*args.values())
+
+
+def test_decode_rejects_on_host(lib):
+    fake = ctypes.c_void_p(0x1000)
+    assert _raw_decode(lib, d=128) == sa.UNSUPPORTED
+    assert _raw_decode(lib, page=8) == sa.UNSUPPORTED
+    assert _raw_decode(lib, hq=6, hkv=4) == sa.INVALID_ARGUMENT
+    assert _raw_decode(lib, pages=0) == sa.INVALID_ARGUMENT
+    assert _raw_decode(lib, scale=float("nan")) == sa.INVALID_ARGUMENT
+    assert _raw_decode(lib) == sa.INVALID_ARGUMENT                       # null pointers
+    odd = ctypes.c_void_p(0x1008)
+    assert _raw_decode(lib, q=odd, k=fake, v=fake, table=fake, lens=fake, sinks=fake,
+                       out=fake) == sa.INVALID_ARGUMENT                  # misaligned q
+    assert _raw_decode(lib, batch=0) == sa.OK                            # nothing to do
+
+
+def test_prefill_rejects_on_host(lib):
+    assert lib.sinkattn_prefill(None, None, None, None, 1, 16, 16, None, 0.125, None, None,
+                                8, 1, 128, None) == sa.UNSUPPORTED
+    assert lib.sinkattn_prefill(None, None, None, None, 1, 16, 16, None, 0.125, None, None,
+                                8, 1, 64, None) == sa.INVALID_ARGUMENT
+    assert lib.sinkattn_prefill_paged(None, None, 1, 16, 16, None, None, None, 1, None, 1, 16,
+                                      None, 0.125, None, None, 8, 1, 64, 32,
+                                      None) == sa.UNSUPPORTED
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(sa, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(sa, "_lib", None)
+    with pytest.raises(RuntimeError):
+        sa.load()
