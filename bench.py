@@ -1,0 +1,486 @@
+#!/usr/bin/env python
+"""Benchmark of the sink-attention hot path on GB300.
+
+Headline (one JSON line on rank 0): paged decode of the gpt-oss-20b-shaped
+batch -- 64 query / 8 KV heads, head_dim 64, 64 requests with kv_len uniform
+in [1, 4096], bf16 paged KV (16-token pages, shuffled), sinks ~ N(0, 2) with
+-inf and +8 heads -- in algorithmic KV GB/s, with its roofline fraction
+against the measured HBM copy bandwidth.  Extra sections time the other
+workloads of the same path (long-context split-KV decode, ragged causal
+prefill in TFLOP/s, the mixed serving batch) and the float64 CPU oracle.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Inputs are synthetic, seeded and resident in HBM before timing (``value``);
+``e2e`` repeats the decode through the public API with pinned host buffers
+and the per-step copies inside the timed region.  Two copies of the KV pool
+alternate between steps, so no step finds the previous step's KV in L2.
+Under torchrun each rank runs its own seeded batch (weak scaling, no
+collective on the data path); rank 0 prints the max-over-ranks time.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "sink-attn decode KV GB/s (% of HBM peak); prefill TFLOP/s (% BF16 peak)"
+HEAD_DIM = 64
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+DECODE_WORKLOAD = ("gpt-oss-20b decode: 64 q / 8 KV heads, head_dim 64, batch 64, "
+                   "kv_len U[1,4096], bf16 paged KV (page 16, shuffled), sinks N(0,2) with -inf/+8 heads")
+
+
+# ----------------------------------------------------------------- helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def decode_bytes(kv_lens, num_qo_heads, num_kv_heads, head_dim=HEAD_DIM, page_size=16):
+    """Algorithmic bytes of one decode pass: every K and V row once, plus q,
+    out, lse, sinks, kv_lens and the page-table entries in use."""
+    kv = sum(int(n) for n in kv_lens)
+    pages = sum((int(n) + page_size - 1) // page_size for n in kv_lens)
+    b = len(kv_lens)
+    return (kv * num_kv_heads * head_dim * 2 * 2          # K and V, bf16
+            + 2 * b * num_qo_heads * head_dim * 2          # q in, out
+            + b * num_qo_heads * 4 + num_qo_heads * 4      # lse, sinks
+            + b * 4 + pages * 4)                           # kv_lens, table
+
+
+def prefill_flops(seqlens, num_qo_heads, head_dim=HEAD_DIM):
+    """QK^T and PV over the causal (lower-triangular incl. diagonal) pairs."""
+    return sum(4 * head_dim * num_qo_heads * n * (n + 1) // 2 for n in seqlens)
+
+
+def extend_flops(q_lens, kv_lens, num_qo_heads, head_dim=HEAD_DIM):
+    tot = 0
+    for lq, lk in zip(q_lens, kv_lens):
+        prefix = lk - lq
+        tot += 4 * head_dim * num_qo_heads * (lq * prefix + lq * (lq + 1) // 2)
+    return tot
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0, period_ms=100):
+        self.index, self.period = index, period_ms
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", f"-lms={self.period}"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def __exit__(self, *exc):
+        time.sleep(0.15)
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.file.close()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.file.name) as f:
+                for line in f:
+                    parts = [x.strip() for x in line.split(",")]
+                    if len(parts) == 9 and parts[1].replace(".", "").isdigit():
+                        rows.append(parts)
+        finally:
+            os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, val in zip(names, r[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())
+                if any(r[3].replace(".", "").isdigit() for r in rows) else None}
+
+
+# ------------------------------------------------------------ distributed
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(backend):
+    import torch.distributed as dist
+    world, rank, _ = dist_info()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend, rank=rank, world_size=world)
+    return world, rank
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def reduce_scalar(x, op, device="cpu"):
+    """All-reduce one float (MAX or SUM) across ranks; identity when alone."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def aggregate(units_this_rank, seconds_this_rank, device="cpu"):
+    """Whole-job throughput: units of all ranks / slowest rank's time."""
+    t = reduce_scalar(seconds_this_rank, "max", device)
+    u = reduce_scalar(units_this_rank, "sum", device)
+    return u, t, (u / t if t > 0 else 0.0)
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def _time_steps(torch, fn, steps, warmup, stream):
+    for i in range(warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        fn(i)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / 1e3
+
+
+def run_decode_arm(args, rank, dev):
+    import torch
+
+    import gqa_attention_learned_gb300 as sa
+    from gqa_attention_learned_gb300 import workloads
+
+    w = workloads.decode_batch(seed=1 + 1000 * rank)
+    hq, hkv = w["num_qo_heads"], w["num_kv_heads"]
+    lens = [int(x) for x in w["kv_lens"]]
+    nbytes = decode_bytes(lens, hq, hkv)
+    q = w["q"].to(dev)
+    pools = [(w["k_cache"].to(dev), w["v_cache"].to(dev))]
+    pools.append((pools[0][0].clone(), pools[0][1].clone()))
+    table, kv_lens, sinks = w["page_table"].to(dev), w["kv_lens"].to(dev), w["sinks"].to(dev)
+    max_kv = w["max_kv_len"]
+    splits, ws_bytes = sa.decode_plan(64, hq, hkv, max_kv, args.splits)
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[0], hq, dtype=torch.float32, device=dev)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        kc, vc = pools[i & 1]
+        sa.decode(q, kc, vc, table, kv_lens, sinks, w["scale"], max_kv, out=out, lse=lse,
+                  num_splits=args.splits, workspace=ws, stream=stream)
+
+    with ClockSampler(index=torch.cuda.current_device()) as clocks:
+        secs = _time_steps(torch, step, args.steps, args.warmup, stream)
+    units, t_max, gbps = aggregate(nbytes * args.steps, secs, dev)
+    launches_per_step = 1 + (1 if splits > 1 else 0)
+
+    # end to end through the public call: pinned host inputs in, results out
+    q_h = w["q"].pin_memory()
+    table_h, lens_h, sinks_h = (w["page_table"].pin_memory(), w["kv_lens"].pin_memory(),
+                                w["sinks"].pin_memory())
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, table_h, lens_h, sinks_h))
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+
+    def e2e_step(i):
+        q.copy_(q_h, non_blocking=True)
+        table.copy_(table_h, non_blocking=True)
+        kv_lens.copy_(lens_h, non_blocking=True)
+        sinks.copy_(sinks_h, non_blocking=True)
+        step(i)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    e2e_steps = max(10, args.steps // 10)
+    e2e_secs = _time_steps(torch, e2e_step, e2e_steps, args.warmup, stream)
+    _, e2e_t, e2e_gbps = aggregate(nbytes * e2e_steps, e2e_secs, dev)
+
+    # same, with the whole paged KV pool copied host -> device every step
+    k_h, v_h = w["k_cache"].pin_memory(), w["v_cache"].pin_memory()
+    kv_pool_bytes = 2 * k_h.numel() * k_h.element_size()
+
+    def e2e_kv_step(i):
+        kc, vc = pools[i & 1]
+        kc.copy_(k_h, non_blocking=True)
+        vc.copy_(v_h, non_blocking=True)
+        e2e_step(i)
+
+    kv_steps = max(5, args.steps // 200)
+    kv_secs = _time_steps(torch, e2e_kv_step, kv_steps, 2, stream)
+    _, _, kv_gbps = aggregate(nbytes * kv_steps, kv_secs, dev)
+
+    return dict(w=w, nbytes=nbytes, secs=t_max, gbps=gbps / 1e9, splits=splits,
+                launches_per_step=launches_per_step, clocks=clocks.summary(),
+                e2e=dict(value=e2e_gbps / 1e9, unit="GB/s", h2d_bytes_per_step=h2d,
+                         d2h_bytes_per_step=d2h, steps=e2e_steps,
+                         note="paged KV cache resident on the device (serving state); per-step "
+                              "q, page table, kv_lens, sinks in and out, lse back"),
+                e2e_kv_h2d=dict(value=kv_gbps / 1e9, unit="GB/s",
+                                h2d_bytes_per_step=h2d + kv_pool_bytes, d2h_bytes_per_step=d2h,
+                                steps=kv_steps))
+
+
+def run_long_decode(args, rank, dev):
+    import torch
+
+    import gqa_attention_learned_gb300 as sa
+    from gqa_attention_learned_gb300 import workloads
+
+    w = workloads.long_decode(seed=2 + 1000 * rank)
+    hq, hkv = w["num_qo_heads"], w["num_kv_heads"]
+    lens = [int(x) for x in w["kv_lens"]]
+    nbytes = decode_bytes(lens, hq, hkv)
+    args_d = [w[n].to(dev) for n in ("q", "k_cache", "v_cache", "page_table", "kv_lens", "sinks")]
+    res = {}
+    for label, splits in (("auto", 0), ("8", 8)):
+        s, ws_bytes = sa.decode_plan(len(lens), hq, hkv, w["max_kv_len"], splits)
+        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+        out = torch.empty_like(args_d[0])
+        lse = torch.empty(len(lens), hq, dtype=torch.float32, device=dev)
+        stream = torch.cuda.current_stream()
+
+        def step(i, splits=splits, ws=ws, out=out, lse=lse):
+            sa.decode(*args_d, w["scale"], w["max_kv_len"], out=out, lse=lse, num_splits=splits,
+                      workspace=ws, stream=stream)
+
+        steps = max(20, args.steps // 50)
+        secs = _time_steps(torch, step, steps, args.warmup, stream)
+        _, t, gbps = aggregate(nbytes * steps, secs, dev)
+        res[label] = dict(splits=s, ms_per_step=1e3 * t / steps, value=gbps / 1e9, unit="GB/s")
+    del args_d
+    torch.cuda.empty_cache()
+    return dict(workload="long-context split-KV decode: 64 q / 8 KV heads, batch 8, "
+                         "kv_len U[32768,131072], bf16 paged KV (page 16)",
+                kv_bytes=nbytes, runs=res)
+
+
+def gpu_arm(args):
+    import torch
+
+    world, rank, local = dist_info()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist_init("nccl" if world > 1 else "gloo")
+    import gqa_attention_learned_gb300 as sa
+    sa.load()
+    peaks, peak_src = load_peaks()
+
+    d = run_decode_arm(args, rank, dev)
+    ms = 1e3 * d["secs"] / args.steps
+    kernel_gbps = d["nbytes"] / (d["secs"] / args.steps) / 1e9     # per launch, this rank
+    extra = {}
+    if not args.quick:
+        extra["long_decode"] = run_long_decode(args, rank, dev)
+    line = {
+        "metric": METRIC, "value": round(d["gbps"], 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 q/k/v, shuffled page pool)",
+        "config": {"workload": DECODE_WORKLOAD, "batch": 64, "num_qo_heads": 64,
+                   "num_kv_heads": 8, "head_dim": 64, "page_size": 16,
+                   "kv_tokens": sum(int(x) for x in d["w"]["kv_lens"]),
+                   "num_splits": d["splits"],
+                   "l2": "inputs larger than L2: two KV pool copies (2 x 671 MB) alternate"},
+        "pct_of_hbm_peak": round(100 * d["gbps"] / peaks["hbm_gbs"], 2),
+        "roofline": {"bound": "hbm", "achieved": round(kernel_gbps, 2),
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(kernel_gbps / peaks["hbm_gbs"], 4),
+                     "traffic": None, "peak_source": peak_src,
+                     "kernel": "decode_kernel (+ merge_kernel when split)",
+                     "bytes_per_launch": d["nbytes"]},
+        "e2e": d["e2e"], "e2e_kv_h2d": d["e2e_kv_h2d"],
+        "gpu_launches": args.steps * d["launches_per_step"],
+        "clocks": d["clocks"],
+        "extra": extra,
+    }
+    if rank == 0 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------- CPU oracle
+
+def oracle_worker(spec):
+    """Runs in a fresh single-threaded process: the float64 oracle, as it
+    stands, decoding (request, KV head) groups of the gpt-oss-20b batch in
+    turn.  spec: warmup/steps/units_per_step, or budget_s (run until spent)."""
+    import numpy as np
+
+    import oracle
+    from gqa_attention_learned_gb300 import workloads
+
+    class Pool:  # float64 view of a bf16 pool, converted row by row on gather
+        def __init__(self, t):
+            self.t, self.shape = t, tuple(t.shape)
+
+        def __getitem__(self, idx):
+            import torch
+            idx = tuple(torch.as_tensor(i) if isinstance(i, np.ndarray) else i for i in idx)
+            return self.t[idx].float().numpy().astype(np.float64)
+
+    w = workloads.decode_batch(seed=1)
+    hq, hkv = w["num_qo_heads"], w["num_kv_heads"]
+    g = hq // hkv
+    q = w["q"].float().numpy().astype(np.float64)
+    table, lens = w["page_table"].numpy(), w["kv_lens"].numpy()
+    sinks = w["sinks"].numpy().astype(np.float64)
+    pools = [(Pool(w["k_cache"][:, h:h + 1]), Pool(w["v_cache"][:, h:h + 1])) for h in range(hkv)]
+    units = [(b, h) for b in range(len(lens)) for h in range(hkv)]
+    cursor = [0]
+
+    def step(n):
+        nbytes = 0
+        for _ in range(n):
+            b, h = units[cursor[0] % len(units)]
+            cursor[0] += 1
+            kc, vc = pools[h]
+            oracle.decode(q[b:b + 1, g * h:g * (h + 1)], kc, vc, table[b:b + 1], lens[b:b + 1],
+                          sinks[g * h:g * (h + 1)], w["scale"])
+            nbytes += decode_bytes(lens[b:b + 1], g, 1)
+        return nbytes
+
+    per = int(spec.get("units_per_step", 1))
+    for _ in range(int(spec.get("warmup", 0))):
+        step(per)
+    t0 = time.perf_counter()
+    done, steps = 0, 0
+    while True:
+        done += step(per)
+        steps += 1
+        el = time.perf_counter() - t0
+        if spec.get("steps") and steps >= spec["steps"]:
+            break
+        if not spec.get("steps") and el >= spec.get("budget_s", 10.0):
+            break
+    return dict(bytes=done, seconds=el, steps=steps, units=steps * per)
+
+
+def _run_oracle(spec):
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--oracle-worker",
+                        json.dumps(spec)], env=env, capture_output=True, text=True, timeout=900)
+    if r.returncode != 0:
+        raise RuntimeError(r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline(budget_s=15.0):
+    """The float64 oracle on one host core (BLAS pinned to one thread in a
+    fresh process) over (request, KV head) groups of the same batch."""
+    res = _run_oracle({"budget_s": budget_s, "units_per_step": 8})
+    return {"value": round(res["bytes"] / res["seconds"] / 1e9, 5), "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"{res['units']} (request, KV head) groups of the gpt-oss-20b decode batch, "
+                      f"cycled in order, {res['seconds']:.1f} s, float64 NumPy, 1 BLAS thread",
+            "host_cores": os.cpu_count()}
+
+
+def reference_arm(args):
+    """The oracle as the reference arm: W untimed steps, then exactly K timed
+    steps, each step a bounded sample of the decode batch ((request, KV head)
+    groups), sized from a probe so the whole run ends within a few minutes."""
+    world, rank, _ = dist_info()
+    if rank != 0:
+        return
+    probe = _run_oracle({"steps": 8, "units_per_step": 1})
+    t_unit = probe["seconds"] / probe["steps"]
+    budget = 100.0
+    per = max(1, int(budget / (args.steps + args.warmup) / t_unit))
+    res = _run_oracle({"warmup": args.warmup, "steps": args.steps, "units_per_step": per})
+    value = res["bytes"] / res["seconds"] / 1e9
+    sample = f"{per} (request, KV head) group(s) of the gpt-oss-20b decode batch per step, cycled"
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s",
+            "n_gpus": world, "steps": res["steps"], "warmup": args.warmup,
+            "ms_per_step": round(1e3 * res["seconds"] / res["steps"], 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) bf16 q/k/v, shuffled page pool)",
+            "config": {"workload": DECODE_WORKLOAD, "sample": sample},
+            "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--splits", type=int, default=0, help="decode split count (0 = planned)")
+    ap.add_argument("--quick", action="store_true", help="headline decode only")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--oracle-worker", default=None, help=argparse.SUPPRESS)
+    args = ap.parse_args()
+    if args.oracle_worker is not None:
+        print(json.dumps(oracle_worker(json.loads(args.oracle_worker))))
+        return
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()
