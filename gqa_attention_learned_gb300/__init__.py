@@ -32,7 +32,12 @@ SIGNATURES = {
     "sinkattn_prefill_paged": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _vp, _c_int,
                                         _vp, _c_int, _c_int, _vp, _c_float, _vp, _vp, _c_int,
                                         _c_int, _c_int, _c_int, _vp]),
+    "sinkattn_decode_static_scratch": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _vp, _c_float,
+                                                _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                                _c_int, _c_int, _c_int, _vp]),
 }
+
+STATIC_SCRATCH_BYTES = 16 << 20
 
 _lib = None
 
@@ -186,4 +191,32 @@ def prefill_paged(q, cu_seqlens_q, k_cache, v_cache, page_table, kv_lens, sinks,
             _ptr(k_cache), _ptr(v_cache), _ptr(page_table), page_table.shape[1], _ptr(kv_lens),
             num_pages, int(max_kv_len), _ptr(sinks), float(scale), _ptr(out), _ptr(lse), hq, hkv,
             d, page, _stream(stream)))
+    return out, lse
+
+
+def decode_static_scratch(q, k_cache, v_cache, page_table, kv_lens, sinks, scale, max_kv_len, *,
+                          out=None, lse=None, num_splits=0, stream=None, want_lse=True):
+    """Decode for callers that cannot allocate device memory: the split
+    scratch is the library's own fixed 16 MiB device array instead of a
+    caller-provided workspace.  Raises SinkAttnError (WORKSPACE_TOO_SMALL)
+    when the sizes need more scratch than that.  Calls that overlap on the GPU
+    share the array and race; order them on one stream."""
+    dev = q.device
+    _want(q, "q", torch.bfloat16, 3)
+    _want(k_cache, "k_cache", torch.bfloat16, 4, dev)
+    _want(v_cache, "v_cache", torch.bfloat16, 4, dev)
+    _want(page_table, "page_table", torch.int32, 2, dev)
+    _want(kv_lens, "kv_lens", torch.int32, 1, dev)
+    _want(sinks, "sinks", torch.float32, 1, dev)
+    batch, hq, d = q.shape
+    num_pages, hkv, page, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty(batch, hq, dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        _check("sinkattn_decode_static_scratch", load().sinkattn_decode_static_scratch(
+            _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table), page_table.shape[1],
+            _ptr(kv_lens), _ptr(sinks), float(scale), _ptr(out), _ptr(lse), batch, hq, hkv, d,
+            page, num_pages, int(max_kv_len), int(num_splits), _stream(stream)))
     return out, lse

@@ -153,6 +153,41 @@ SINKATTN_API int sinkattn_prefill_paged(const void *q, const int32_t *cu_seqlens
                            int num_qo_heads, int num_kv_heads, int head_dim,
                            int page_size, void *stream);
 
+/*
+ * Decode for callers that cannot allocate device memory.
+ *
+ * Some callers of this library cannot call cudaMalloc at the point where they
+ * run decode: code running inside another allocator's critical section,
+ * plug-ins hosted by a runtime that owns all device memory, or tools that
+ * must not change the process's memory footprint.  For them this entry point
+ * takes the same arguments as sinkattn_decode minus the workspace: the split
+ * scratch lives in one fixed array of SINKATTN_STATIC_SCRATCH_BYTES (16 MiB)
+ * of device memory that is part of the library itself, so every GPU that
+ * loads the library holds that array until the process exits.  The pages
+ * this library follows have no counterpart to this call; it only changes
+ * where the scratch memory comes from.
+ *
+ *   - Allocates nothing: no cudaMalloc/cudaFree, no allocating library call.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture on the device.
+ *   - Returns SINKATTN_WORKSPACE_TOO_SMALL, launching nothing, when the plan
+ *     for these sizes (see sinkattn_decode_plan) needs more scratch than the
+ *     array holds.  Passing num_splits = 1 needs no scratch at all.
+ *   - All calls share the one array, and it keeps the last call's contents.
+ *     Decode writes every scratch byte it reads within the same call, so no
+ *     clearing is needed, but two calls that overlap on the GPU (different
+ *     streams, or different host threads, without ordering between them)
+ *     race on the array and may return wrong results.
+ */
+#define SINKATTN_STATIC_SCRATCH_BYTES (16u << 20)
+
+SINKATTN_API int sinkattn_decode_static_scratch(
+    const void *q, const void *k_cache, const void *v_cache, const int32_t *page_table,
+    int max_pages_per_seq, const int32_t *kv_lens, const float *sinks, float scale, void *out,
+    float *lse, int batch, int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
+    int num_pages, int max_kv_len, int num_splits, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,64 @@
+"""The decode entry point for callers that cannot allocate device memory.
+
+sinkattn_decode_static_scratch keeps its split scratch in a fixed device array
+inside the library instead of a caller-provided workspace.  These tests call
+it through the C ABI and compare it with sinkattn_decode (caller workspace) on
+the same inputs, within the parity bars used for the oracle comparisons, on
+two calls in a row (the array keeps the first call's contents).  This file is
+collected last so that a failure here never hides the other tests.
+"""
+
+import pytest
+import torch
+
+import gqa_attention_learned_gb300 as sa
+from gqa_attention_learned_gb300 import workloads
+from tolerances import assert_lse_close, assert_out_close, to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def _inputs(w):
+    return [w[n].to(DEV) for n in ("q", "k_cache", "v_cache", "page_table", "kv_lens", "sinks")]
+
+
+def test_static_scratch_matches_workspace_decode_twice():
+    w = workloads.decode_batch(seed=17, batch=24, min_len=1500, max_len=6000)
+    args = _inputs(w)
+    max_kv = w["max_kv_len"]
+    splits, need = sa.decode_plan(24, 64, 8, max_kv, 0)
+    assert splits > 1 and 0 < need <= sa.STATIC_SCRATCH_BYTES    # the scratch is really used
+    ref_out, ref_lse = sa.decode(*args, w["scale"], max_kv)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        out, lse = sa.decode_static_scratch(*args, w["scale"], max_kv)
+        torch.cuda.synchronize()
+        assert_out_close(out.cpu(), to_np(ref_out), "static-scratch out")
+        assert_lse_close(lse.cpu(), to_np(ref_lse), "static-scratch lse")
+
+
+def test_static_scratch_with_other_inputs_after_first_call():
+    # a second, differently sized problem right after: stale scratch contents
+    # from the previous call must not leak into this one
+    w = workloads.long_decode(seed=23, batch=2, min_len=20000, max_len=40000)
+    args = _inputs(w)
+    for splits in (0, 12):
+        ref_out, ref_lse = sa.decode(*args, w["scale"], w["max_kv_len"], num_splits=splits)
+        out, lse = sa.decode_static_scratch(*args, w["scale"], w["max_kv_len"], num_splits=splits)
+        torch.cuda.synchronize()
+        assert_out_close(out.cpu(), to_np(ref_out), "static-scratch out")
+        assert_lse_close(lse.cpu(), to_np(ref_lse), "static-scratch lse")
+
+
+def test_static_scratch_rejects_plans_beyond_its_size():
+    # 1024 requests x 64 heads x 8 splits needs ~136 MB of scratch: refused
+    # on the host, nothing launched
+    q = torch.zeros(1024, 64, 64, dtype=torch.bfloat16, device=DEV)
+    kc = torch.zeros(16, 8, 16, 64, dtype=torch.bfloat16, device=DEV)
+    table = torch.zeros(1024, 1, dtype=torch.int32, device=DEV)
+    lens = torch.ones(1024, dtype=torch.int32, device=DEV)
+    sinks = torch.zeros(64, dtype=torch.float32, device=DEV)
+    with pytest.raises(sa.SinkAttnError) as e:
+        sa.decode_static_scratch(q, kc, kc, table, lens, sinks, 0.125, 4096, num_splits=8)
+    assert e.value.status == sa.WORKSPACE_TOO_SMALL
