@@ -1,0 +1,376 @@
+// Causal prefill (ragged, or appended to a paged KV prefix) with learned
+// sinks on the 5th-generation tensor cores (tcgen05 + tensor memory).
+//
+// Operation: "GPT-OSS on day 0" (Perplexity blog), section "Kernels for
+// GPT-OSS / Sink Attention" -- each head's running max starts at its sink and
+// its running sum at 1, so the sink joins the softmax denominator without a
+// value row.  Query i of a request with kv_len keys and q_len new queries
+// sees keys j <= kv_len - q_len + i (for plain prefill kv_len = q_len).
+//
+// One CTA = one 128-row query tile of one query head (6 warps):
+//   warp 4      TMA producer: the Q tile once, then K/V tiles of 128 keys
+//               into a 2-stage ring (contiguous: one 16 KB box each; paged:
+//               eight 2 KB page boxes each), 128-byte swizzle.
+//   warp 5      MMA issuer (one thread): S = Q K^T (tcgen05.mma, A and B
+//               from shared memory, M=128 N=128 K=16 x4) into tensor memory;
+//               then O_j = P V (A = P from tensor memory, B = V from shared
+//               memory in MN-major layout, M=128 N=64 K=16 x8).
+//   warps 0..3  softmax, one thread per query row (= tensor-memory lane):
+//               S from tensor memory, online softmax in base 2 started at
+//               the sink, P (bf16) back into tensor memory, and the running
+//               output kept in registers: O <- O * alpha + O_j.
+// Tensor memory per CTA: S 128 columns, P 64, O_j 64 = 256, so two CTAs share
+// an SM and their MMA and softmax phases interleave.  Heavier query tiles
+// (later ones, which see more keys) are launched first.
+// V rows past a request's last key are zeroed in shared memory before the PV
+// MMA (0 * NaN would poison whole rows); score columns past a row's causal
+// limit are masked by index.
+
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+#include <cmath>
+
+namespace sa {
+namespace {
+
+constexpr int kBM = 128;                       // query rows per CTA
+constexpr int kBN = 128;                       // keys per KV tile
+constexpr int kStages = 2;
+constexpr int kTileBytes = kBN * kHeadDim * 2;    // 16 KB
+constexpr int kThreads = 192;
+constexpr int kProducerWarp = 4, kMmaWarp = 5;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColS = 0, kColP = 128, kColO = 192;
+
+constexpr int kOffQ = 0;
+constexpr int kOffStage = kTileBytes;                       // K then V per stage
+constexpr int kOffBars = kOffStage + kStages * 2 * kTileBytes;
+constexpr int kSmemBytes = kOffBars + 256 + 1024;           // barriers + alignment slack
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t kv_full[kStages];
+  uint64_t kv_empty[kStages];
+  uint64_t s_full;
+  uint64_t p_full;
+  uint64_t o_final;
+  uint32_t tmem_base;
+  int bad;
+};
+static_assert(sizeof(Bars) <= 256, "barrier block");
+
+constexpr uint32_t kIdescQK = umma_idesc_bf16(128, 128, false, false);
+constexpr uint32_t kIdescPV = umma_idesc_bf16(128, 64, false, true);
+
+__device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+template <bool kPaged>
+__global__ void __launch_bounds__(kThreads, 2)
+prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+               const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
+  const int per_tile = p.num_seqs * p.num_qo_heads;
+  const int qt = p.num_q_tiles - 1 - static_cast<int>(blockIdx.x / per_tile);
+  const int rem = static_cast<int>(blockIdx.x % per_tile);
+  const int head = rem % p.num_qo_heads;
+  const int seq = rem / p.num_qo_heads;
+  const int kvh = head / p.group;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- request geometry and argument checks (uniform over the CTA)
+  const int q_start = p.cu_seqlens_q[seq];
+  const int q_end = p.cu_seqlens_q[seq + 1];
+  const int q_len = q_end - q_start;
+  int kv_len, k_start = 0;
+  if constexpr (kPaged) {
+    kv_len = p.kv_lens[seq];
+  } else {
+    k_start = p.cu_seqlens_k[seq];
+    kv_len = p.cu_seqlens_k[seq + 1] - k_start;
+  }
+  bool bad = q_start < 0 || q_len < 0 || q_end > p.total_q || q_len > p.max_q_len ||
+             kv_len < q_len || kv_len > p.max_kv_len;
+  if constexpr (kPaged) {
+    bad = bad || cdiv(kv_len, kPageSize) > p.max_pages_per_seq;
+  } else {
+    bad = bad || k_start < 0 || k_start + kv_len > p.total_k;
+  }
+  if (bad) {
+    // Poison every row this request owns that lies inside the buffers.
+    if (qt != 0 || q_start < 0 || q_start >= p.total_q) return;
+    const int stop = min(max(q_end, q_start), p.total_q);
+    for (int t = q_start + threadIdx.x; t < stop; t += kThreads) {
+      uint4 nan4 = make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
+      uint4 *dst = reinterpret_cast<uint4 *>(p.out + (static_cast<size_t>(t) * p.num_qo_heads + head) * kHeadDim);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) dst[i] = nan4;
+      if (p.lse) p.lse[static_cast<size_t>(t) * p.num_qo_heads + head] = NAN;
+    }
+    return;
+  }
+  const int i0 = qt * kBM;
+  if (i0 >= q_len) return;
+  const int rows = min(kBM, q_len - i0);
+  const int shift = kv_len - q_len;                        // bottom-right causal offset
+  const int key_end = shift + i0 + rows;                   // keys needed, exclusive (<= kv_len)
+  const int n_tiles = cdiv(key_end, kBN);
+  const int npages = cdiv(kv_len, kPageSize);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  Bars &bar = *reinterpret_cast<Bars *>(smem + kOffBars);
+  uint8_t *sQ = smem + kOffQ;
+  auto sK = [&](int s) { return smem + kOffStage + s * 2 * kTileBytes; };
+  auto sV = [&](int s) { return smem + kOffStage + s * 2 * kTileBytes + kTileBytes; };
+
+  if (warp == kMmaWarp) {
+    tmem_alloc(&bar.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == kProducerWarp * 32) {
+    mbar_init(&bar.q_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bar.kv_full[s], 1);
+      mbar_init(&bar.kv_empty[s], 1);
+    }
+    mbar_init(&bar.s_full, 1);
+    mbar_init(&bar.p_full, kBM);
+    mbar_init(&bar.o_final, 1);
+    bar.bad = 0;
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bar.tmem_base;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&qmap);
+      tma_prefetch_desc(&kmap);
+      tma_prefetch_desc(&vmap);
+      mbar_arrive_expect_tx(&bar.q_full, kBM * kHeadDim * 2);
+      tma_load_3d(sQ, &qmap, &bar.q_full, 0, head, q_start + i0);
+    }
+    const int32_t *table = kPaged ? p.page_table + static_cast<size_t>(seq) * p.max_pages_per_seq : nullptr;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int s = j % kStages;
+      if (j >= kStages &&
+          !__all_sync(0xffffffffu, mbar_wait(&bar.kv_empty[s], ((j / kStages) + 1) & 1))) {
+        if (lane == 0) atomicOr(&bar.bad, 1);
+        break;
+      }
+      if constexpr (kPaged) {
+        // lanes 0..7 each own one 16-token page of the 128-key tile
+        const int pg = j * (kBN / kPageSize) + lane;
+        int pid = -1;
+        if (lane < kBN / kPageSize && pg < npages) pid = table[pg];
+        const bool ok = pid >= 0 && pid < p.num_pages;
+        if (lane < kBN / kPageSize && pg < npages && !ok) atomicOr(&bar.bad, 1);
+        const unsigned mask = __ballot_sync(0xffffffffu, ok);
+        if (lane == 0) mbar_arrive_expect_tx(&bar.kv_full[s], __popc(mask) * 2 * kPageSize * kHeadDim * 2);
+        __syncwarp();
+        if (ok) {
+          const int off = lane * kPageSize * kHeadDim * 2;
+          tma_load_3d(sK(s) + off, &kmap, &bar.kv_full[s], 0, kvh * kPageSize, pid);
+          tma_load_3d(sV(s) + off, &vmap, &bar.kv_full[s], 0, kvh * kPageSize, pid);
+        }
+      } else {
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bar.kv_full[s], 2 * kTileBytes);
+          tma_load_3d(sK(s), &kmap, &bar.kv_full[s], 0, kvh, k_start + j * kBN);
+          tma_load_3d(sV(s), &vmap, &bar.kv_full[s], 0, kvh, k_start + j * kBN);
+        }
+      }
+      __syncwarp();
+    }
+  } else if (warp == kMmaWarp) {
+    // ----------------------------------------------------------------- MMA
+    const uint32_t tS = tmem + kColS, tP = tmem + kColP, tO = tmem + kColO;
+    bool ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_full, 0));
+    const uint64_t dq = umma_desc_sw128(smem_u32(sQ), 16, 1024);
+    auto issue_qk = [&](int j) -> bool {
+      const int s = j % kStages;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bar.kv_full[s], (j / kStages) & 1))) return false;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint64_t dk = umma_desc_sw128(smem_u32(sK(s)), 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kHeadDim / 16; ++kk)
+          umma_ss(tS, dq + 2 * kk, dk + 2 * kk, kIdescQK, kk > 0);   // +32 bytes per k-step
+        umma_commit(&bar.s_full);
+      }
+      __syncwarp();
+      return true;
+    };
+    if (ok) ok = issue_qk(0);
+    for (int j = 0; ok && j < n_tiles; ++j) {
+      const int s = j % kStages;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bar.p_full, j & 1))) { ok = false; break; }
+      tc_fence_after();
+      const int valid = kv_len - j * kBN;        // keys of this tile inside the request
+      if (valid < kBN) {
+        // zero V rows [valid, 128): whole 128-byte rows, so the swizzle is irrelevant
+        uint4 *v = reinterpret_cast<uint4 *>(sV(s));
+        for (int idx = max(valid, 0) * 8 + lane; idx < kBN * 8; idx += 32) v[idx] = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (lane == 0) {
+        const uint64_t dv = umma_desc_sw128(smem_u32(sV(s)), kTileBytes, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          umma_ts(tO, tP + 8 * kk, dv + (2048 >> 4) * kk, kIdescPV, kk > 0);   // 16 keys = 2 KB
+        umma_commit(&bar.kv_empty[s]);
+      }
+      __syncwarp();
+      if (j + 1 < n_tiles && !issue_qk(j + 1)) { ok = false; break; }
+    }
+    if (!ok && lane == 0) atomicOr(&bar.bad, 1);
+    if (lane == 0) umma_commit(&bar.o_final);
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------- softmax
+    const int r = threadIdx.x;                          // row = TMEM lane
+    const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const int i = i0 + r;
+    const int limit = min(shift + i + 1, kv_len);       // keys [0, limit) visible
+    const float sl2 = p.scale_log2;
+    float m = p.sinks[head] * kLog2e;
+    float d = 1.f;
+    float alpha_prev = 1.f;
+    float o[kHeadDim];
+#pragma unroll
+    for (int c = 0; c < kHeadDim; ++c) o[c] = 0.f;
+    bool ok = true;
+
+    auto fold = [&](float alpha) {
+      uint32_t x[32];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        tmem_ld32(trow + kColO + 32 * h, x);
+        tmem_ld_wait32(x);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) o[32 * h + c] = fmaf(o[32 * h + c], alpha, __uint_as_float(x[c]));
+      }
+    };
+
+    for (int j = 0; j < n_tiles; ++j) {
+      // warp-uniform: the tcgen05.ld/st below are .sync.aligned
+      if (!__all_sync(0xffffffffu, mbar_wait(&bar.s_full, j & 1))) { ok = false; break; }
+      tc_fence_after();
+      if (j > 0) fold(alpha_prev);
+      const int k0 = j * kBN;
+      const bool need_mask = k0 + kBN > limit;
+      float mx = -INFINITY;
+      uint32_t x[32];
+#pragma unroll
+      for (int c = 0; c < kBN / 32; ++c) {
+        tmem_ld32(trow + kColS + 32 * c, x);
+        tmem_ld_wait32(x);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          float v = __uint_as_float(x[e]) * sl2;
+          if (need_mask && k0 + 32 * c + e >= limit) v = -INFINITY;
+          mx = fmaxf(mx, v);
+        }
+      }
+      const float m_new = fmaxf(m, mx);
+      const float mu = m_new == -INFINITY ? 0.f : m_new;
+      const float alpha = ex2(m - mu);
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < kBN / 32; ++c) {
+        tmem_ld32(trow + kColS + 32 * c, x);
+        tmem_ld_wait32(x);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float p0 = ex2(fmaf(__uint_as_float(x[e]), sl2, -mu));
+          float p1 = ex2(fmaf(__uint_as_float(x[e + 1]), sl2, -mu));
+          if (need_mask) {
+            if (k0 + 32 * c + e >= limit) p0 = 0.f;
+            if (k0 + 32 * c + e + 1 >= limit) p1 = 0.f;
+          }
+          sum += p0 + p1;
+          pk[e / 2] = pack_bf16(p0, p1);
+        }
+        tmem_st16(trow + kColP + 16 * c, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bar.p_full);
+      d = d * alpha + sum;
+      m = m_new;
+      alpha_prev = alpha;
+    }
+    if (__all_sync(0xffffffffu, mbar_wait(&bar.o_final, 0))) {
+      tc_fence_after();
+      if (ok && n_tiles > 0) fold(alpha_prev);
+    } else {
+      ok = false;
+    }
+    if (!ok) atomicOr(&bar.bad, 1);
+
+    // outputs are written after the CTA-wide barrier below
+    __syncthreads();
+    const bool failed = bar.bad != 0;
+    if (r < rows) {
+      const size_t row = static_cast<size_t>(q_start + i) * p.num_qo_heads + head;
+      const float inv = d > 0.f ? 1.f / d : 0.f;
+      uint4 *dst = reinterpret_cast<uint4 *>(p.out + row * kHeadDim);
+#pragma unroll
+      for (int c = 0; c < kHeadDim / 8; ++c) {
+        uint4 w;
+        if (failed) {
+          w = make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
+        } else {
+          w.x = pack_bf16(o[8 * c + 0] * inv, o[8 * c + 1] * inv);
+          w.y = pack_bf16(o[8 * c + 2] * inv, o[8 * c + 3] * inv);
+          w.z = pack_bf16(o[8 * c + 4] * inv, o[8 * c + 5] * inv);
+          w.w = pack_bf16(o[8 * c + 6] * inv, o[8 * c + 7] * inv);
+        }
+        dst[c] = w;
+      }
+      if (p.lse) p.lse[row] = failed ? NAN : (d > 0.f ? (m + lg2(d)) * kLn2 : -INFINITY);
+    }
+    tc_fence_before();
+    __syncthreads();
+    return;
+  }
+  __syncthreads();          // matches the softmax warps' output barrier
+  tc_fence_before();
+  __syncthreads();          // everybody is done with tensor memory
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap,
+                           const CUtensorMap &vmap, const PrefillParams &p, cudaStream_t stream) {
+  static_assert(kSmemBytes <= 113 * 1024, "two CTAs per SM");
+  const unsigned long long ctas =
+      static_cast<unsigned long long>(p.num_q_tiles) * p.num_seqs * p.num_qo_heads;
+  if (ctas == 0) return cudaSuccess;
+  if (ctas > 0x7fffffffull) return cudaErrorInvalidConfiguration;
+  cudaError_t err;
+  if (p.paged) {
+    err = cudaFuncSetAttribute(prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kSmemBytes);
+    if (err != cudaSuccess) return err;
+    prefill_kernel<true><<<static_cast<unsigned>(ctas), kThreads, kSmemBytes, stream>>>(qmap, kmap, vmap, p);
+  } else {
+    err = cudaFuncSetAttribute(prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kSmemBytes);
+    if (err != cudaSuccess) return err;
+    prefill_kernel<false><<<static_cast<unsigned>(ctas), kThreads, kSmemBytes, stream>>>(qmap, kmap, vmap, p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace sa

@@ -70,6 +70,25 @@ bool encode_rows_map(CUtensorMap *map, const void *base, unsigned long long rows
   return r == CUDA_SUCCESS;
 }
 
+// bf16 tensor viewed as [d2][d1][64] (128-byte rows), box {64, b1, b2},
+// 128-byte swizzle.
+bool encode_map(CUtensorMap *map, const void *base, unsigned long long d1, unsigned long long d2,
+                unsigned b1, unsigned b2) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), d1, d2};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim * 2),
+                           static_cast<cuuint64_t>(d1 * kHeadDim * 2)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim), b1, b2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+constexpr int kPrefillTile = 128;
+
 struct DecodePlan {
   int num_splits = 1;
   int pages_per_chunk = 1;
@@ -205,13 +224,36 @@ int sinkattn_prefill(const void *q, const void *k, const void *v, const int32_t 
   if (num_seqs < 0 || total_tokens < 0 || max_seqlen < 0 || num_qo_heads <= 0 ||
       num_kv_heads <= 0 || num_qo_heads % num_kv_heads || !std::isfinite(scale))
     return SINKATTN_INVALID_ARGUMENT;
-  if (num_seqs == 0 || total_tokens == 0) return SINKATTN_OK;
+  if (num_seqs == 0 || total_tokens == 0 || max_seqlen == 0) return SINKATTN_OK;
   if (!q || !k || !v || !cu_seqlens || !sinks || !out) return SINKATTN_INVALID_ARGUMENT;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
       !aligned(cu_seqlens, 4) || !aligned(sinks, 4) || (lse && !aligned(lse, 4)))
     return SINKATTN_INVALID_ARGUMENT;
-  (void)stream;
-  return SINKATTN_UNSUPPORTED;
+  CUtensorMap qmap, kmap, vmap;
+  if (!encode_map(&qmap, q, num_qo_heads, total_tokens, 1, kPrefillTile) ||
+      !encode_map(&kmap, k, num_kv_heads, total_tokens, 1, kPrefillTile) ||
+      !encode_map(&vmap, v, num_kv_heads, total_tokens, 1, kPrefillTile))
+    return SINKATTN_CUDA_ERROR;
+  sa::PrefillParams p{};
+  p.q = static_cast<const uint16_t *>(q);
+  p.cu_seqlens_q = cu_seqlens;
+  p.cu_seqlens_k = cu_seqlens;
+  p.sinks = sinks;
+  p.out = static_cast<uint16_t *>(out);
+  p.lse = lse;
+  p.scale_log2 = scale * sa::kLog2e;
+  p.num_seqs = num_seqs;
+  p.total_q = total_tokens;
+  p.total_k = total_tokens;
+  p.max_q_len = max_seqlen;
+  p.max_kv_len = max_seqlen;
+  p.num_qo_heads = num_qo_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = num_qo_heads / num_kv_heads;
+  p.paged = 0;
+  p.num_q_tiles = ceil_div(max_seqlen, kPrefillTile);
+  cudaError_t err = sa::launch_prefill(qmap, kmap, vmap, p, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? SINKATTN_OK : SINKATTN_CUDA_ERROR;
 }
 
 int sinkattn_prefill_paged(const void *q, const int32_t *cu_seqlens_q, int num_seqs, int total_q,
@@ -221,11 +263,46 @@ int sinkattn_prefill_paged(const void *q, const int32_t *cu_seqlens_q, int num_s
                            const float *sinks, float scale, void *out, float *lse,
                            int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
                            void *stream) {
-  (void)q; (void)cu_seqlens_q; (void)num_seqs; (void)total_q; (void)max_q_len; (void)k_cache;
-  (void)v_cache; (void)page_table; (void)max_pages_per_seq; (void)kv_lens; (void)num_pages;
-  (void)max_kv_len; (void)sinks; (void)scale; (void)out; (void)lse; (void)num_qo_heads;
-  (void)num_kv_heads; (void)head_dim; (void)page_size; (void)stream;
-  return SINKATTN_UNSUPPORTED;
+  if (head_dim != kHeadDim || page_size != kPageSize) return SINKATTN_UNSUPPORTED;
+  if (num_seqs < 0 || total_q < 0 || max_q_len < 0 || max_kv_len < 0 || num_qo_heads <= 0 ||
+      num_kv_heads <= 0 || num_qo_heads % num_kv_heads || num_pages <= 0 ||
+      max_pages_per_seq <= 0 || !std::isfinite(scale))
+    return SINKATTN_INVALID_ARGUMENT;
+  if (num_seqs == 0 || total_q == 0 || max_q_len == 0) return SINKATTN_OK;
+  if (!q || !cu_seqlens_q || !k_cache || !v_cache || !page_table || !kv_lens || !sinks || !out)
+    return SINKATTN_INVALID_ARGUMENT;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(cu_seqlens_q, 4) || !aligned(page_table, 4) || !aligned(kv_lens, 4) ||
+      !aligned(sinks, 4) || (lse && !aligned(lse, 4)))
+    return SINKATTN_INVALID_ARGUMENT;
+  CUtensorMap qmap, kmap, vmap;
+  const unsigned long long rows = static_cast<unsigned long long>(num_kv_heads) * kPageSize;
+  if (!encode_map(&qmap, q, num_qo_heads, total_q, 1, kPrefillTile) ||
+      !encode_map(&kmap, k_cache, rows, num_pages, kPageSize, 1) ||
+      !encode_map(&vmap, v_cache, rows, num_pages, kPageSize, 1))
+    return SINKATTN_CUDA_ERROR;
+  sa::PrefillParams p{};
+  p.q = static_cast<const uint16_t *>(q);
+  p.cu_seqlens_q = cu_seqlens_q;
+  p.page_table = page_table;
+  p.kv_lens = kv_lens;
+  p.sinks = sinks;
+  p.out = static_cast<uint16_t *>(out);
+  p.lse = lse;
+  p.scale_log2 = scale * sa::kLog2e;
+  p.num_seqs = num_seqs;
+  p.total_q = total_q;
+  p.max_q_len = max_q_len;
+  p.max_kv_len = max_kv_len;
+  p.num_qo_heads = num_qo_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = num_qo_heads / num_kv_heads;
+  p.max_pages_per_seq = max_pages_per_seq;
+  p.num_pages = num_pages;
+  p.paged = 1;
+  p.num_q_tiles = ceil_div(max_q_len, kPrefillTile);
+  cudaError_t err = sa::launch_prefill(qmap, kmap, vmap, p, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? SINKATTN_OK : SINKATTN_CUDA_ERROR;
 }
 
 }  // extern "C"
