@@ -307,6 +307,104 @@ def run_long_decode(args, rank, dev):
                 kv_bytes=nbytes, runs=res)
 
 
+def run_prefill(args, rank, dev, peaks):
+    import torch
+
+    import gqa_attention_learned_gb300 as sa
+    from gqa_attention_learned_gb300 import workloads
+
+    w = workloads.ragged_prefill(seed=3 + 1000 * rank)
+    cu = [int(x) for x in w["cu_seqlens"]]
+    lens = [b - a for a, b in zip(cu, cu[1:])]
+    flops = prefill_flops(lens, w["num_qo_heads"])
+    args_d = [w[n].to(dev) for n in ("q", "k", "v", "cu_seqlens", "sinks")]
+    out = torch.empty_like(args_d[0])
+    lse = torch.empty(args_d[0].shape[0], w["num_qo_heads"], dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        sa.prefill(*args_d, w["scale"], w["max_seqlen"], out=out, lse=lse, stream=stream)
+
+    steps = max(10, args.steps // 200)
+    secs = _time_steps(torch, step, steps, args.warmup, stream)
+    _, t, fps = aggregate(flops * steps, secs, dev)
+    tf = fps / 1e12
+    return dict(workload="causal ragged prefill: 64 q / 8 KV heads, head_dim 64, 4 sequences "
+                         f"{lens} ({sum(lens)} tokens), bf16, fp32 LSE",
+                flops_per_step=flops, steps=steps, ms_per_step=1e3 * t / steps,
+                value=round(tf, 2), unit="TFLOP/s",
+                roofline={"bound": "tensor", "achieved": round(tf, 2),
+                          "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                          "frac": round(tf / peaks["bf16_tflops"], 4),
+                          "frac_of_sustained": round(tf / peaks["bf16_tflops_sustained"], 4),
+                          "traffic": None, "kernel": "prefill_kernel<false>"})
+
+
+def run_mixed(args, rank, dev, peaks):
+    import torch
+
+    import gqa_attention_learned_gb300 as sa
+    from gqa_attention_learned_gb300 import workloads
+
+    m = workloads.mixed_batch(seed=4 + 1000 * rank)
+    d, e = m["decode"], m["extend"]
+    hq, hkv = m["num_qo_heads"], m["num_kv_heads"]
+    kc, vc, sinks = m["k_cache"].to(dev), m["v_cache"].to(dev), m["sinks"].to(dev)
+    dq, dt, dl = d["q"].to(dev), d["page_table"].to(dev), d["kv_lens"].to(dev)
+    eq, ecu, et, el = (e["q"].to(dev), e["cu_seqlens_q"].to(dev), e["page_table"].to(dev),
+                       e["kv_lens"].to(dev))
+    dec_lens = [int(x) for x in d["kv_lens"]]
+    ext_kv = [int(x) for x in e["kv_lens"]]
+    ext_q = [e["max_q_len"]] * len(ext_kv)
+    nbytes = decode_bytes(dec_lens, hq, hkv)
+    flops = extend_flops(ext_q, ext_kv, hq)
+    _, ws_bytes = sa.decode_plan(len(dec_lens), hq, hkv, d["max_kv_len"], 0)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    dout = torch.empty_like(dq)
+    dlse = torch.empty(dq.shape[0], hq, dtype=torch.float32, device=dev)
+    eout = torch.empty_like(eq)
+    else_ = torch.empty(eq.shape[0], hq, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    steps = max(10, args.steps // 200)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+
+    def step(i, record=False):
+        if record:
+            ev[i][0].record(stream)
+        sa.decode(dq, kc, vc, dt, dl, sinks, m["scale"], d["max_kv_len"], out=dout, lse=dlse,
+                  workspace=ws, stream=stream)
+        if record:
+            ev[i][1].record(stream)
+        sa.prefill_paged(eq, ecu, kc, vc, et, el, sinks, m["scale"], e["max_q_len"],
+                         e["max_kv_len"], out=eout, lse=else_, stream=stream)
+        if record:
+            ev[i][2].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    barrier()
+    for i in range(steps):
+        step(i, record=True)
+    torch.cuda.synchronize()
+    t_dec = sum(ev[i][0].elapsed_time(ev[i][1]) for i in range(steps)) / 1e3
+    t_ext = sum(ev[i][1].elapsed_time(ev[i][2]) for i in range(steps)) / 1e3
+    t_all = sum(ev[i][0].elapsed_time(ev[i][2]) for i in range(steps)) / 1e3
+    _, t_all, _ = aggregate(0, t_all, dev)
+    dec_gbs = nbytes * steps / t_dec / 1e9
+    ext_tf = flops * steps / t_ext / 1e12
+    ideal = nbytes / (peaks["hbm_gbs"] * 1e9) + flops / (peaks["bf16_tflops"] * 1e12)
+    return dict(workload="mixed serving batch: 32 decode requests (kv_len U[512,16384]) + 4 "
+                         "chunked-prefill requests of 2048 tokens on prefixes U[0,14336], one "
+                         "shuffled page pool, two launches on one stream",
+                steps=steps, ms_per_step=1e3 * t_all / steps,
+                decode={"value": round(dec_gbs, 2), "unit": "GB/s", "bytes": nbytes,
+                        "ms": 1e3 * t_dec / steps},
+                extend={"value": round(ext_tf, 2), "unit": "TFLOP/s", "flops": flops,
+                        "ms": 1e3 * t_ext / steps},
+                combined_roofline_frac=round(ideal / (t_all / steps), 4))
+
+
 def gpu_arm(args):
     import torch
 
@@ -318,12 +416,18 @@ def gpu_arm(args):
     sa.load()
     peaks, peak_src = load_peaks()
 
+    sections = set(args.sections.split(","))
     d = run_decode_arm(args, rank, dev)
     ms = 1e3 * d["secs"] / args.steps
     kernel_gbps = d["nbytes"] / (d["secs"] / args.steps) / 1e9     # per launch, this rank
     extra = {}
     if not args.quick:
-        extra["long_decode"] = run_long_decode(args, rank, dev)
+        if "long" in sections:
+            extra["long_decode"] = run_long_decode(args, rank, dev)
+        if "prefill" in sections:
+            extra["prefill"] = run_prefill(args, rank, dev, peaks)
+        if "mixed" in sections:
+            extra["mixed"] = run_mixed(args, rank, dev, peaks)
     line = {
         "metric": METRIC, "value": round(d["gbps"], 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
@@ -467,6 +571,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--splits", type=int, default=0, help="decode split count (0 = planned)")
     ap.add_argument("--quick", action="store_true", help="headline decode only")
+    ap.add_argument("--sections", default="long,prefill,mixed",
+                    help="extra sections after the headline decode")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--oracle-worker", default=None, help=argparse.SUPPRESS)
