@@ -13,13 +13,14 @@
 //               eight 2 KB page boxes each), 128-byte swizzle.
 //   warp 5      MMA issuer (one thread): S = Q K^T (tcgen05.mma, A and B
 //               from shared memory, M=128 N=128 K=16 x4) into tensor memory;
-//               then O_j = P V (A = P from tensor memory, B = V from shared
+//               then O += P V (A = P from tensor memory, B = V from shared
 //               memory in MN-major layout, M=128 N=64 K=16 x8).
 //   warps 0..3  softmax, one thread per query row (= tensor-memory lane):
-//               S from tensor memory, online softmax in base 2 started at
-//               the sink, P (bf16) back into tensor memory, and the running
-//               output kept in registers: O <- O * alpha + O_j.
-// Tensor memory per CTA: S 128 columns, P 64, O_j 64 = 256, so two CTAs share
+//               S from tensor memory (read once per tile), online softmax in
+//               base 2 started at the sink, P (bf16) back into tensor memory;
+//               O accumulates in tensor memory across KV tiles and is
+//               rescaled only when a row max grows by more than 2^8.
+// Tensor memory per CTA: S 128 columns, P 64, O 64 = 256, so two CTAs share
 // an SM and their MMA and softmax phases interleave.  Heavier query tiles
 // (later ones, which see more keys) are launched first.
 // V rows past a request's last key are zeroed in shared memory before the PV
@@ -42,6 +43,7 @@ constexpr int kThreads = 192;
 constexpr int kProducerWarp = 4, kMmaWarp = 5;
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColS = 0, kColP = 128, kColO = 192;
+constexpr float kRescaleLog2 = 8.f;     // lazy O rescale threshold (P < 256)
 
 constexpr int kOffQ = 0;
 constexpr int kOffStage = kTileBytes;                       // K then V per stage
@@ -222,7 +224,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         const uint64_t dv = umma_desc_sw128(smem_u32(sV(s)), kTileBytes, 1024);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          umma_ts(tO, tP + 8 * kk, dv + (2048 >> 4) * kk, kIdescPV, kk > 0);   // 16 keys = 2 KB
+          umma_ts(tO, tP + 8 * kk, dv + (2048 >> 4) * kk, kIdescPV, (j > 0) || (kk > 0));  // 16 keys = 2 KB
         umma_commit(&bar.kv_empty[s]);
       }
       __syncwarp();
@@ -238,77 +240,108 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const int i = i0 + r;
     const int limit = min(shift + i + 1, kv_len);       // keys [0, limit) visible
     const float sl2 = p.scale_log2;
+    const bool pos_scale = sl2 >= 0.f;
+    // Masked scores are replaced (by index, so NaN keys cannot leak) with the
+    // raw value whose scaled logit is -inf.
+    const uint32_t masked_raw = pos_scale ? 0xff800000u : 0x7f800000u;
+    // m is the reference max (base 2) that P and the tensor-memory O are
+    // relative to.  It starts at the sink (so the sink's term in d is 1) and
+    // only moves when a row max exceeds it by more than kRescaleLog2, at which
+    // point O and d are rescaled; out = O/d and lse = m + log2(d) are exact
+    // for any reference, and P stays below 2^kRescaleLog2.
     float m = p.sinks[head] * kLog2e;
     float d = 1.f;
-    float alpha_prev = 1.f;
-    float o[kHeadDim];
-#pragma unroll
-    for (int c = 0; c < kHeadDim; ++c) o[c] = 0.f;
     bool ok = true;
-
-    auto fold = [&](float alpha) {
-      uint32_t x[32];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        tmem_ld32(trow + kColO + 32 * h, x);
-        tmem_ld_wait32(x);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) o[32 * h + c] = fmaf(o[32 * h + c], alpha, __uint_as_float(x[c]));
-      }
-    };
+    uint32_t x[4][32];
 
     for (int j = 0; j < n_tiles; ++j) {
       // warp-uniform: the tcgen05.ld/st below are .sync.aligned
       if (!__all_sync(0xffffffffu, mbar_wait(&bar.s_full, j & 1))) { ok = false; break; }
       tc_fence_after();
-      if (j > 0) fold(alpha_prev);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(trow + kColS + 32 * c, x[c]);
+      tmem_ld_wait32(x[0]);
+      reg_tie32(x[1]);
+      reg_tie32(x[2]);
+      reg_tie32(x[3]);
       const int k0 = j * kBN;
-      const bool need_mask = k0 + kBN > limit;
+      if (__any_sync(0xffffffffu, k0 + kBN > limit)) {   // only tiles on the causal edge
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (k0 + 32 * c + e >= limit) x[c][e] = masked_raw;
+      }
       float mx = -INFINITY;
-      uint32_t x[32];
+      if (pos_scale) {
 #pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) {
-        tmem_ld32(trow + kColS + 32 * c, x);
-        tmem_ld_wait32(x);
+        for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float v = __uint_as_float(x[e]) * sl2;
-          if (need_mask && k0 + 32 * c + e >= limit) v = -INFINITY;
-          mx = fmaxf(mx, v);
-        }
+          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(x[c][e]));
+        mx *= sl2;
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(x[c][e]) * sl2);
       }
       const float m_new = fmaxf(m, mx);
-      const float mu = m_new == -INFINITY ? 0.f : m_new;
-      const float alpha = ex2(m - mu);
+      float alpha = 1.f;
+      bool rescale = false;
+      if (j == 0) {                        // O holds nothing yet: just re-base d
+        if (m_new != -INFINITY) {
+          d *= ex2(m - m_new);
+          m = m_new;
+        }
+      } else if (m_new > m + kRescaleLog2) {
+        alpha = ex2(m - m_new);
+        d *= alpha;
+        m = m_new;
+        rescale = true;
+      }
+      const float mu = m == -INFINITY ? 0.f : m;
       float sum = 0.f;
 #pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) {
-        tmem_ld32(trow + kColS + 32 * c, x);
-        tmem_ld_wait32(x);
-        uint32_t pk[16];
+      for (int c = 0; c < 4; ++c) {
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float p0 = ex2(fmaf(__uint_as_float(x[e]), sl2, -mu));
-          float p1 = ex2(fmaf(__uint_as_float(x[e + 1]), sl2, -mu));
-          if (need_mask) {
-            if (k0 + 32 * c + e >= limit) p0 = 0.f;
-            if (k0 + 32 * c + e + 1 >= limit) p1 = 0.f;
-          }
+        for (int e = 0; e < 16; ++e) {
+          const float p0 = ex2(fmaf(__uint_as_float(x[c][2 * e]), sl2, -mu));
+          const float p1 = ex2(fmaf(__uint_as_float(x[c][2 * e + 1]), sl2, -mu));
           sum += p0 + p1;
-          pk[e / 2] = pack_bf16(p0, p1);
+          x[c][e] = pack_bf16(p0, p1);         // pairs packed in place
         }
-        tmem_st16(trow + kColP + 16 * c, pk);
+        tmem_st16(trow + kColP + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&x[c][0]));
       }
+      d += sum;
       tmem_st_wait();
+      if (__any_sync(0xffffffffu, rescale)) {
+        // rare: scale this row's O (finished by the previous PV; the next PV
+        // is issued only after p_full below)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) tmem_ld32(trow + kColO + 32 * h, x[h]);
+        tmem_ld_wait32(x[0]);
+        reg_tie32(x[1]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) x[h][e] = __float_as_uint(__uint_as_float(x[h][e]) * alpha);
+        tmem_st16(trow + kColO, *reinterpret_cast<uint32_t(*)[16]>(&x[0][0]));
+        tmem_st16(trow + kColO + 16, *reinterpret_cast<uint32_t(*)[16]>(&x[0][16]));
+        tmem_st16(trow + kColO + 32, *reinterpret_cast<uint32_t(*)[16]>(&x[1][0]));
+        tmem_st16(trow + kColO + 48, *reinterpret_cast<uint32_t(*)[16]>(&x[1][16]));
+        tmem_st_wait();
+      }
       tc_fence_before();
       mbar_arrive(&bar.p_full);
-      d = d * alpha + sum;
-      m = m_new;
-      alpha_prev = alpha;
     }
     if (__all_sync(0xffffffffu, mbar_wait(&bar.o_final, 0))) {
       tc_fence_after();
-      if (ok && n_tiles > 0) fold(alpha_prev);
+      if (ok && n_tiles > 0) {
+        tmem_ld32(trow + kColO, x[0]);
+        tmem_ld32(trow + kColO + 32, x[1]);
+        tmem_ld_wait32(x[0]);
+        reg_tie32(x[1]);
+      }
     } else {
       ok = false;
     }
@@ -321,16 +354,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       const size_t row = static_cast<size_t>(q_start + i) * p.num_qo_heads + head;
       const float inv = d > 0.f ? 1.f / d : 0.f;
       uint4 *dst = reinterpret_cast<uint4 *>(p.out + row * kHeadDim);
+      auto o = [&](int c) { return __uint_as_float(x[c >> 5][c & 31]) * inv; };
 #pragma unroll
       for (int c = 0; c < kHeadDim / 8; ++c) {
         uint4 w;
         if (failed) {
           w = make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
         } else {
-          w.x = pack_bf16(o[8 * c + 0] * inv, o[8 * c + 1] * inv);
-          w.y = pack_bf16(o[8 * c + 2] * inv, o[8 * c + 3] * inv);
-          w.z = pack_bf16(o[8 * c + 4] * inv, o[8 * c + 5] * inv);
-          w.w = pack_bf16(o[8 * c + 6] * inv, o[8 * c + 7] * inv);
+          w.x = pack_bf16(o(8 * c + 0), o(8 * c + 1));
+          w.y = pack_bf16(o(8 * c + 2), o(8 * c + 3));
+          w.z = pack_bf16(o(8 * c + 4), o(8 * c + 5));
+          w.w = pack_bf16(o(8 * c + 6), o(8 * c + 7));
         }
         dst[c] = w;
       }
