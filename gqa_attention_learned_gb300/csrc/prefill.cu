@@ -67,6 +67,51 @@ constexpr uint32_t kIdescPV = umma_idesc_bf16(128, 64, false, true);
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
+// 2^x on the FMA pipe, for the share of the softmax exponentials that the
+// MUFU unit does not take.  Range reduction x = n + f with n = round(x) (the
+// 1.5 * 2^23 shifter leaves n in the low mantissa bits of t), f in [-1/2, 1/2];
+// 2^f by a cubic with minimax relative error 7.5e-5 (Remez exchange, see
+// gen_exp2_poly.py), far below bf16's 2^-9 rounding of P; 2^n is added to
+// the exponent field.  Inputs below -125 are clamped there (result ~2e-38,
+// i.e. 0 next to any unmasked term) so the exponent sum stays a normal number.
+#ifndef SA_POLY_NUM
+#define SA_POLY_NUM 0        // SA_POLY_NUM of every 8 exponentials use the polynomial
+#endif
+constexpr float kP0 = 0.99992806f, kP1 = 0.69326097f, kP2 = 0.24261113f, kP3 = 0.05517167f;
+
+__device__ __forceinline__ float exp2_poly(float x) {
+  x = fmaxf(x, -125.f);
+  const float t = x + 12582912.f;
+  const float n = t - 12582912.f;
+  const float f = x - n;
+  const float p = fmaf(fmaf(fmaf(kP3, f, kP2), f, kP1), f, kP0);
+  return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
+}
+
+template <int E>
+__device__ __forceinline__ float exp2_mixed(float x) {
+  if constexpr ((E & 7) < SA_POLY_NUM) return exp2_poly(x);
+  else return ex2(x);
+}
+
+// P = 2^(s * sl2 - mu) for 32 scores, packed as bf16 pairs into r[0..15];
+// the pair sums accumulate in `acc` (fp32x2).
+template <int E = 0>
+__device__ __forceinline__ void pack_chunk(uint32_t (&r)[32], uint64_t scale2, uint64_t negmu2,
+                                           uint64_t &acc) {
+  if constexpr (E < 16) {
+    float x0, x1;
+    f2_unpack(f2_fma(f2_pack(__uint_as_float(r[2 * E]), __uint_as_float(r[2 * E + 1])), scale2,
+                     negmu2),
+              x0, x1);
+    const float p0 = exp2_mixed<2 * E>(x0);
+    const float p1 = exp2_mixed<2 * E + 1>(x1);
+    acc = f2_add(acc, f2_pack(p0, p1));
+    r[E] = pack_bf16(p0, p1);
+    pack_chunk<E + 1>(r, scale2, negmu2, acc);
+  }
+}
+
 template <bool kPaged>
 __global__ void __launch_bounds__(kThreads, 2)
 prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
@@ -272,14 +317,20 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
           for (int e = 0; e < 32; ++e)
             if (k0 + 32 * c + e >= limit) x[c][e] = masked_raw;
       }
-      float mx = -INFINITY;
+      float mx;
       if (pos_scale) {
+        float mc[4];                          // four independent chains
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 4; ++c) {
+          mc[c] = __uint_as_float(x[c][0]);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(x[c][e]));
-        mx *= sl2;
+          for (int e = 1; e < 31; e += 2)
+            mc[c] = fmax3(mc[c], __uint_as_float(x[c][e]), __uint_as_float(x[c][e + 1]));
+          mc[c] = fmaxf(mc[c], __uint_as_float(x[c][31]));
+        }
+        mx = fmax3(mc[0], mc[1], fmaxf(mc[2], mc[3])) * sl2;
       } else {
+        mx = -INFINITY;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -300,19 +351,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         rescale = true;
       }
       const float mu = m == -INFINITY ? 0.f : m;
-      float sum = 0.f;
+      const uint64_t scale2 = f2_pack(sl2, sl2), negmu2 = f2_pack(-mu, -mu);
+      uint64_t acc[4];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2(fmaf(__uint_as_float(x[c][2 * e]), sl2, -mu));
-          const float p1 = ex2(fmaf(__uint_as_float(x[c][2 * e + 1]), sl2, -mu));
-          sum += p0 + p1;
-          x[c][e] = pack_bf16(p0, p1);         // pairs packed in place
-        }
+        acc[c] = 0;                                   // (+0.f, +0.f)
+        pack_chunk(x[c], scale2, negmu2, acc[c]);     // pairs packed in place
         tmem_st16(trow + kColP + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&x[c][0]));
       }
-      d += sum;
+      float s0, s1;
+      f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), s0, s1);
+      d += s0 + s1;
       tmem_st_wait();
       if (__any_sync(0xffffffffu, rescale)) {
         // rare: scale this row's O (finished by the previous PV; the next PV
