@@ -22,6 +22,7 @@ _c_int, _c_float, _c_size, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_size_t, 
 SIGNATURES = {
     "sinkattn_status_string": (ctypes.c_char_p, [_c_int]),
     "sinkattn_version": (_c_int, []),
+    "sinkattn_last_error": (ctypes.c_char_p, []),
     "sinkattn_decode_plan": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                       ctypes.POINTER(_c_int), ctypes.POINTER(_c_size)]),
     "sinkattn_decode": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _vp, _c_float, _vp, _vp,
@@ -45,7 +46,10 @@ _lib = None
 class SinkAttnError(RuntimeError):
     def __init__(self, fn, status):
         self.status = status
-        super().__init__(f"{fn} failed: {status_string(status)} ({status})")
+        detail = ""
+        if status == CUDA_ERROR:
+            detail = ": " + load().sinkattn_last_error().decode()
+        super().__init__(f"{fn} failed: {status_string(status)} ({status}){detail}")
 
 
 def load():

@@ -8,6 +8,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstdio>
 #include <atomic>
 #include <cmath>
 #include <mutex>
@@ -47,6 +48,21 @@ int device_sm_count() {
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
   if (dev >= 0 && dev < kMaxDevices) cache[dev].store(n, std::memory_order_relaxed);
   return n;
+}
+
+thread_local char g_last_error[256] = "";
+
+// Record the CUDA error behind a SINKATTN_CUDA_ERROR for sinkattn_last_error.
+int cuda_status(cudaError_t err, const char *where) {
+  if (err == cudaSuccess) return SINKATTN_OK;
+  snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%d)", where, cudaGetErrorString(err),
+           static_cast<int>(err));
+  return SINKATTN_CUDA_ERROR;
+}
+
+int fail_msg(const char *what) {
+  snprintf(g_last_error, sizeof(g_last_error), "%s", what);
+  return SINKATTN_CUDA_ERROR;
 }
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -137,6 +153,8 @@ const char *sinkattn_status_string(int status) {
 
 int sinkattn_version(void) { return 100; }
 
+const char *sinkattn_last_error(void) { return g_last_error; }
+
 int sinkattn_decode_plan(int batch, int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
                          int max_kv_len, int num_sms, int *num_splits, size_t *workspace_bytes) {
   if (!num_splits || !workspace_bytes) return SINKATTN_INVALID_ARGUMENT;
@@ -146,7 +164,7 @@ int sinkattn_decode_plan(int batch, int num_qo_heads, int num_kv_heads, int head
     return SINKATTN_INVALID_ARGUMENT;
   if (num_sms == 0) {
     num_sms = device_sm_count();
-    if (num_sms == 0) return SINKATTN_CUDA_ERROR;
+    if (num_sms == 0) return fail_msg("no CUDA device to plan for");
   }
   const DecodePlan plan = plan_decode(batch, num_qo_heads, num_kv_heads, max_kv_len, num_sms, *num_splits);
   *num_splits = plan.num_splits;
@@ -178,7 +196,7 @@ int sinkattn_decode(const void *q, const void *k_cache, const void *v_cache,
     return SINKATTN_UNSUPPORTED;
 
   const int sms = device_sm_count();
-  if (sms == 0) return SINKATTN_CUDA_ERROR;
+  if (sms == 0) return fail_msg("no CUDA device (SM count query failed)");
   const DecodePlan plan = plan_decode(batch, num_qo_heads, num_kv_heads, max_kv_len, sms, num_splits);
   if (plan.num_splits > 1) {
     if (!workspace || workspace_bytes < plan.workspace_bytes) return SINKATTN_WORKSPACE_TOO_SMALL;
@@ -189,7 +207,7 @@ int sinkattn_decode(const void *q, const void *k_cache, const void *v_cache,
   const unsigned long long rows = static_cast<unsigned long long>(num_kv_heads) * kPageSize;
   if (!encode_rows_map(&kmap, k_cache, rows, num_pages, kPageSize) ||
       !encode_rows_map(&vmap, v_cache, rows, num_pages, kPageSize))
-    return SINKATTN_CUDA_ERROR;
+    return fail_msg("cuTensorMapEncodeTiled failed");
 
   sa::DecodeParams p{};
   p.q = static_cast<const uint16_t *>(q);
@@ -212,8 +230,8 @@ int sinkattn_decode(const void *q, const void *k_cache, const void *v_cache,
   p.num_pages = num_pages;
   p.num_splits = plan.num_splits;
   p.pages_per_chunk = plan.pages_per_chunk;
-  cudaError_t err = sa::launch_decode(kmap, vmap, p, static_cast<cudaStream_t>(stream));
-  return err == cudaSuccess ? SINKATTN_OK : SINKATTN_CUDA_ERROR;
+  return cuda_status(sa::launch_decode(kmap, vmap, p, static_cast<cudaStream_t>(stream)),
+                     "decode launch");
 }
 
 int sinkattn_prefill(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
@@ -233,7 +251,7 @@ int sinkattn_prefill(const void *q, const void *k, const void *v, const int32_t 
   if (!encode_map(&qmap, q, num_qo_heads, total_tokens, 1, kPrefillTile) ||
       !encode_map(&kmap, k, num_kv_heads, total_tokens, 1, kPrefillTile) ||
       !encode_map(&vmap, v, num_kv_heads, total_tokens, 1, kPrefillTile))
-    return SINKATTN_CUDA_ERROR;
+    return fail_msg("cuTensorMapEncodeTiled failed");
   sa::PrefillParams p{};
   p.q = static_cast<const uint16_t *>(q);
   p.cu_seqlens_q = cu_seqlens;
@@ -251,9 +269,9 @@ int sinkattn_prefill(const void *q, const void *k, const void *v, const int32_t 
   p.num_kv_heads = num_kv_heads;
   p.group = num_qo_heads / num_kv_heads;
   p.paged = 0;
-  p.num_q_tiles = ceil_div(max_seqlen, kPrefillTile);
-  cudaError_t err = sa::launch_prefill(qmap, kmap, vmap, p, static_cast<cudaStream_t>(stream));
-  return err == cudaSuccess ? SINKATTN_OK : SINKATTN_CUDA_ERROR;
+  p.num_q_tiles = ceil_div(max_seqlen, 2 * kPrefillTile);   // 256-row work items
+  return cuda_status(sa::launch_prefill(qmap, kmap, vmap, p, static_cast<cudaStream_t>(stream)),
+                     "prefill launch");
 }
 
 int sinkattn_prefill_paged(const void *q, const int32_t *cu_seqlens_q, int num_seqs, int total_q,
@@ -280,7 +298,7 @@ int sinkattn_prefill_paged(const void *q, const int32_t *cu_seqlens_q, int num_s
   if (!encode_map(&qmap, q, num_qo_heads, total_q, 1, kPrefillTile) ||
       !encode_map(&kmap, k_cache, rows, num_pages, kPageSize, 1) ||
       !encode_map(&vmap, v_cache, rows, num_pages, kPageSize, 1))
-    return SINKATTN_CUDA_ERROR;
+    return fail_msg("cuTensorMapEncodeTiled failed");
   sa::PrefillParams p{};
   p.q = static_cast<const uint16_t *>(q);
   p.cu_seqlens_q = cu_seqlens_q;
@@ -300,9 +318,9 @@ int sinkattn_prefill_paged(const void *q, const int32_t *cu_seqlens_q, int num_s
   p.max_pages_per_seq = max_pages_per_seq;
   p.num_pages = num_pages;
   p.paged = 1;
-  p.num_q_tiles = ceil_div(max_q_len, kPrefillTile);
-  cudaError_t err = sa::launch_prefill(qmap, kmap, vmap, p, static_cast<cudaStream_t>(stream));
-  return err == cudaSuccess ? SINKATTN_OK : SINKATTN_CUDA_ERROR;
+  p.num_q_tiles = ceil_div(max_q_len, 2 * kPrefillTile);    // 256-row work items
+  return cuda_status(sa::launch_prefill(qmap, kmap, vmap, p, static_cast<cudaStream_t>(stream)),
+                     "prefill launch");
 }
 
 }  // extern "C"

@@ -68,6 +68,10 @@ typedef enum sinkattn_status {
 /* Static description of a status code. */
 SINKATTN_API const char *sinkattn_status_string(int status);
 
+/* Detail of the last SINKATTN_CUDA_ERROR returned on the calling thread
+ * (the CUDA error name and where it happened); "" if none. */
+SINKATTN_API const char *sinkattn_last_error(void);
+
 /* Library version as major*10000 + minor*100 + patch. */
 SINKATTN_API int sinkattn_version(void);
 
