@@ -69,6 +69,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
   }
 }
 
+// Named barrier `id` over `count` threads (a multiple of 32).
+__device__ __forceinline__ void named_barrier_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // -------------------------------------------------------------------- TMA
 // 3-D tiled bulk tensor load global -> shared, completion counted in bytes
 // on an mbarrier.  Coordinates are innermost first.

@@ -103,7 +103,8 @@ bool encode_map(CUtensorMap *map, const void *base, unsigned long long d1, unsig
   return r == CUDA_SUCCESS;
 }
 
-constexpr int kPrefillTile = 128;
+constexpr int kPrefillTile = 128;     // query rows per prefill CTA
+constexpr int kPrefillKvTile = 128;   // keys per prefill K/V tile
 
 struct DecodePlan {
   int num_splits = 1;
@@ -249,8 +250,8 @@ int sinkattn_prefill(const void *q, const void *k, const void *v, const int32_t 
     return SINKATTN_INVALID_ARGUMENT;
   CUtensorMap qmap, kmap, vmap;
   if (!encode_map(&qmap, q, num_qo_heads, total_tokens, 1, kPrefillTile) ||
-      !encode_map(&kmap, k, num_kv_heads, total_tokens, 1, kPrefillTile) ||
-      !encode_map(&vmap, v, num_kv_heads, total_tokens, 1, kPrefillTile))
+      !encode_map(&kmap, k, num_kv_heads, total_tokens, 1, kPrefillKvTile) ||
+      !encode_map(&vmap, v, num_kv_heads, total_tokens, 1, kPrefillKvTile))
     return fail_msg("cuTensorMapEncodeTiled failed");
   sa::PrefillParams p{};
   p.q = static_cast<const uint16_t *>(q);
@@ -269,7 +270,7 @@ int sinkattn_prefill(const void *q, const void *k, const void *v, const int32_t 
   p.num_kv_heads = num_kv_heads;
   p.group = num_qo_heads / num_kv_heads;
   p.paged = 0;
-  p.num_q_tiles = ceil_div(max_seqlen, 2 * kPrefillTile);   // 256-row work items
+  p.num_q_tiles = ceil_div(max_seqlen, kPrefillTile);
   return cuda_status(sa::launch_prefill(qmap, kmap, vmap, p, static_cast<cudaStream_t>(stream)),
                      "prefill launch");
 }
@@ -318,7 +319,7 @@ int sinkattn_prefill_paged(const void *q, const int32_t *cu_seqlens_q, int num_s
   p.max_pages_per_seq = max_pages_per_seq;
   p.num_pages = num_pages;
   p.paged = 1;
-  p.num_q_tiles = ceil_div(max_q_len, 2 * kPrefillTile);    // 256-row work items
+  p.num_q_tiles = ceil_div(max_q_len, kPrefillTile);
   return cuda_status(sa::launch_prefill(qmap, kmap, vmap, p, static_cast<cudaStream_t>(stream)),
                      "prefill launch");
 }
