@@ -103,7 +103,8 @@ def _want(t, name, dtype, dims=None, device=None):
 
 def decode_plan(batch, num_qo_heads, num_kv_heads, max_kv_len, num_splits=0, num_sms=0,
                 head_dim=64, page_size=16):
-    """Split count and workspace bytes that `decode` will use (host only)."""
+    """(workers, workspace bytes) that `decode` will use (host only).  A
+    workspace must be zero-filled before its first use (torch.zeros)."""
     s = _c_int(num_splits)
     w = _c_size(0)
     _check("sinkattn_decode_plan",
@@ -135,7 +136,8 @@ def decode(q, k_cache, v_cache, page_table, kv_lens, sinks, scale, max_kv_len, *
     splits, ws_bytes = decode_plan(batch, hq, hkv, max_kv_len, num_splits, head_dim=d,
                                    page_size=page) if batch else (1, 0)
     if workspace is None and ws_bytes:
-        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        # zero-filled once; decode leaves it ready for the next call
+        workspace = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
     ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
     with torch.cuda.device(dev):
         _check("sinkattn_decode", load().sinkattn_decode(

@@ -1,8 +1,10 @@
 // sinkattn_decode_static_scratch: decode whose split scratch is a fixed
 // device array inside the library, for callers that cannot allocate device
-// memory.  It forwards to sinkattn_decode with that array as the workspace.
+// memory.  It clears the array's merge counters and forwards to
+// sinkattn_decode with that array as the workspace.
 
 #include "sinkattn.h"
+#include "kernels.cuh"
 
 #include <cuda_runtime.h>
 
@@ -55,6 +57,13 @@ extern "C" SINKATTN_API int sinkattn_decode_static_scratch(
   void *scratch = nullptr;
   st = scratch_for_current_device(&scratch);
   if (st != SINKATTN_OK) return st;
+  // the merge counters must start at zero (a memset, not an allocation)
+  const size_t zero_bytes = sa::decode_counter_bytes(batch, num_qo_heads, num_kv_heads);
+  if (zero_bytes &&
+      cudaMemsetAsync(scratch, 0, zero_bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return SINKATTN_CUDA_ERROR;
+  }
   return sinkattn_decode(q, k_cache, v_cache, page_table, max_pages_per_seq, kv_lens, sinks, scale,
                          out, lse, batch, num_qo_heads, num_kv_heads, head_dim, page_size,
                          num_pages, max_kv_len, num_splits, scratch, SINKATTN_STATIC_SCRATCH_BYTES,

@@ -45,21 +45,22 @@ def test_plan_is_host_only_and_deterministic(lib):
     a = sa.decode_plan(64, 64, 8, 4096, num_sms=152)
     b = sa.decode_plan(64, 64, 8, 4096, num_sms=152)
     assert a == b
-    splits, ws = a
-    assert splits >= 1
-    assert (ws == 0) == (splits == 1)
-    # explicit split counts are honoured up to the page count
+    workers, ws = a
+    assert workers == 152 * 2 * 4            # every resident warp slot
+    # counters (64 x 8 units, 256-byte rounded) + 2 chunk slots per worker
+    assert ws == 2048 + 2 * workers * 8 * 64 * 4 + 2 * workers * 8 * 4
+    # explicit worker counts are honoured up to one page per worker
     s, ws = sa.decode_plan(8, 64, 8, 131072, num_splits=8, num_sms=152)
-    assert s == 8 and ws == 8 * 8 * 64 * 65 * 4
+    assert s == 8 and ws == 256 + 2 * 8 * 8 * 64 * 4 + 512
     s, _ = sa.decode_plan(1, 4, 1, 37, num_splits=64, num_sms=152)
-    assert s == 3      # 37 tokens = 3 pages: at most one page per split
+    assert s == 3      # 37 tokens = 3 pages: at most one page per worker
     s, ws = sa.decode_plan(4, 4, 1, 0, num_sms=152)
-    assert s == 1 and ws == 0
+    assert s == 1 and ws > 0
 
 
-def test_plan_long_context_splits(lib):
+def test_plan_long_context_workers(lib):
     s, _ = sa.decode_plan(8, 64, 8, 131072, num_sms=152)
-    assert 8 <= s <= 256
+    assert s == 1216
 
 
 def test_plan_rejects_bad_arguments(lib):
