@@ -20,12 +20,13 @@
 //    online softmax at the sink.
 //  * Each warp runs its own STAGES-deep TMA pipeline: lane 0 issues 3-D bulk
 //    tensor copies of the page's K and V tiles (2 KB each, 128-byte swizzle)
-//    -- plus the unit's 8-head Q tile (1 KB) on the page that starts a chunk
-//    -- onto the stage's mbarrier.
+//    onto the stage's mbarrier; 3 CTAs x 4 warps x 4 stages keep 48 pages
+//    (192 KB) in flight per SM, which is what HBM latency asks for.  The next
+//    unit's Q is loaded into registers one chunk ahead.
 //  * The GQA group shares every K/V tile: S^T[16 tok x 8 heads] = K . Q^T and
 //    O^T[64 x 8] += V^T . P^T, each 4 mma.sync.m16n8k16 (bf16 in, fp32 acc).
 //    P^T goes from the score accumulator layout to the B-operand layout with
-//    movmatrix.trans; K, V^T and Q come from shared memory by ldmatrix,
+//    movmatrix.trans; K and V^T come from shared memory by ldmatrix,
 //    bank-conflict free thanks to the swizzle.  Row maxima take 3 xor-shuffles
 //    per page; running sums stay per lane until the chunk ends.
 // There is no tensor-memory (tcgen05) path here: n = 8 query heads per KV
@@ -42,14 +43,12 @@ namespace {
 constexpr int kNW = 4;                 // worker warps per CTA
 constexpr int kStages = 4;             // pages in flight per warp
 constexpr int kTileBytes = kPageSize * kHeadDim * 2;   // 2048
-constexpr int kQTileBytes = 8 * kHeadDim * 2;          // 1024: 8 query heads
-constexpr int kStageBytes = 2 * kTileBytes + kQTileBytes;
+constexpr int kStageBytes = 2 * kTileBytes;
 constexpr int kHeadsPerTile = 8;
 constexpr int kMaxBatch = 4096;        // requests per launch (per-CTA tables)
 
 constexpr int kOffStages = 0;
-constexpr int kOffStaging = kNW * kStages * kStageBytes;            // per warp 8 x 64 fp32
-constexpr int kOffBars = kOffStaging + kNW * kHeadsPerTile * kHeadDim * 4;
+constexpr int kOffBars = kNW * kStages * kStageBytes;
 constexpr int kOffTables = kOffBars + kNW * kStages * 8;
 constexpr int kSmemFixed = kOffTables + 1024;                       // + alignment slack
 
@@ -85,9 +84,9 @@ __device__ __forceinline__ PageRef locate(long long x, const long long *prefix, 
   return r;
 }
 
-__global__ void __launch_bounds__(kNW * 32)
+__global__ void __launch_bounds__(kNW * 32, 3)
 decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-              const __grid_constant__ CUtensorMap qmap, const DecodeParams p) {
+              const DecodeParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const int units_per_req = p.num_kv_heads * p.head_blocks;
@@ -96,7 +95,6 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
   uint8_t *stages = smem + kOffStages + warp * kStages * kStageBytes;
-  float *staging = reinterpret_cast<float *>(smem + kOffStaging) + warp * kHeadsPerTile * kHeadDim;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBars) + warp * kStages;
   long long *prefix = reinterpret_cast<long long *>(smem + kOffTables);   // [batch + 1]
   int *npages = reinterpret_cast<int *>(prefix + p.batch + 1);           // [batch], -1 = bad
@@ -132,7 +130,6 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
     if (warp == 0) {
       tma_prefetch_desc(&kmap);
       tma_prefetch_desc(&vmap);
-      tma_prefetch_desc(&qmap);
     }
   }
   __syncthreads();
@@ -186,26 +183,21 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       iss_next = load_batch(j + 32);
     }
     const int src = j & 31;
-    const int b = __shfl_sync(0xffffffffu, iss.b, src);
     const int uh = __shfl_sync(0xffffffffu, iss.uh, src);
-    const int pg = __shfl_sync(0xffffffffu, iss.pg, src);
     const int pid = __shfl_sync(0xffffffffu, iss.pid, src);
     if (lane == 0) {
       uint64_t *bar = &bars[j % kStages];
       uint8_t *dst = stages + (j % kStages) * kStageBytes;
-      const bool chunk_start = pg == 0 || j == 0;
-      const int kvh = uh / p.head_blocks, hb = uh % p.head_blocks;
+      const int kvh = uh / p.head_blocks;
       fence_proxy_async_smem();
       if (pid >= 0 && pid < p.num_pages) {
-        mbar_arrive_expect_tx(bar, 2 * kTileBytes + (chunk_start ? kQTileBytes : 0));
+        mbar_arrive_expect_tx(bar, 2 * kTileBytes);
         tma_load_3d(dst, &kmap, bar, 0, kvh * kPageSize, pid);
         tma_load_3d(dst + kTileBytes, &vmap, bar, 0, kvh * kPageSize, pid);
       } else {
         stage_bad |= 1u << (j % kStages);   // skip the copy; the phase still completes
-        mbar_arrive_expect_tx(bar, chunk_start ? kQTileBytes : 0);
+        mbar_arrive(bar);
       }
-      if (chunk_start)
-        tma_load_3d(dst + 2 * kTileBytes, &qmap, bar, 0, kvh * p.group + hb * kHeadsPerTile, b);
     }
   };
 
@@ -217,16 +209,44 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
   const int k_hi = lane >> 4;
   const int v_row = (lane & 7) + 8 * (lane >> 4);
   const int v_hi = (lane >> 3) & 1;
-  const int q_row = lane & 7, q_mat = lane >> 3;
 
   // chunk state (heads 2t, 2t+1 of the current unit)
   float m0 = -INFINITY, m1 = -INFINITY, d0 = 0.f, d1 = 0.f;
   float o[4][4];
-  uint32_t qb[4][2];
+  uint32_t qb[4][2], qn[4][2];             // Q^T B fragments: current / next unit
   int cur_b = -1, cur_uh = 0, chunk_first_pg = 0, cur_pg = 0;
   bool failed = false, chunk_bad = false;
 
-  // Finish the current chunk: full unit -> output; else partial + merge.
+  // Q^T as the B operand for unit (b, uh): lane (g, t) holds query head g of
+  // the unit's 8-head block, dims 16ks+2t.. and 16ks+8+2t..; heads past the
+  // GQA group are zero.  Loaded one unit ahead so the latency stays hidden.
+  auto load_q = [&](int b, int uh, uint32_t (&dst)[4][2]) {
+    const int kvh = uh / p.head_blocks, hb = uh % p.head_blocks;
+    const int nheads = min(kHeadsPerTile, p.group - hb * kHeadsPerTile);
+    const bool live = b >= 0 && b < p.batch && g < nheads;
+    const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+        p.q + (static_cast<size_t>(live ? b : 0) * p.num_qo_heads + kvh * p.group +
+               hb * kHeadsPerTile + (live ? g : 0)) * kHeadDim);
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      dst[ks][0] = live ? __ldg(qrow + 8 * ks + t) : 0u;
+      dst[ks][1] = live ? __ldg(qrow + 8 * ks + 4 + t) : 0u;
+    }
+  };
+  auto next_unit = [&](int b, int uh, int &nb, int &nuh) {
+    nb = b;
+    nuh = uh + 1;
+    if (nuh == units_per_req) {
+      nuh = 0;
+      do { ++nb; } while (nb < p.batch && npages[nb] <= 0);
+    }
+  };
+
+  // Output element (head, dim) of this lane's fragment value v = o[mt][k].
+  auto frag_head = [&](int k) { return 2 * t + (k & 1); };
+  auto frag_dim = [&](int mt, int k) { return 16 * mt + g + 8 * (k >> 1); };
+
+  // Finish the current chunk: whole unit -> output; else chunk + merge.
   auto finish_chunk = [&]() {
     float e0 = d0, e1 = d1;
 #pragma unroll
@@ -240,50 +260,42 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
     const int kvh = cur_uh / p.head_blocks, hb = cur_uh % p.head_blocks;
     const int head0 = kvh * p.group + hb * kHeadsPerTile;
     const int nheads = min(kHeadsPerTile, p.group - hb * kHeadsPerTile);
-    // normalised chunk output into the warp's staging area [head][dim]
     const float i0 = e0 > 0.f ? 1.f / e0 : 0.f, i1 = e1 > 0.f ? 1.f / e1 : 0.f;
-#pragma unroll
-    for (int mt = 0; mt < 4; ++mt) {
-      staging[(2 * t) * kHeadDim + 16 * mt + g] = o[mt][0] * i0;
-      staging[(2 * t + 1) * kHeadDim + 16 * mt + g] = o[mt][1] * i1;
-      staging[(2 * t) * kHeadDim + 16 * mt + 8 + g] = o[mt][2] * i0;
-      staging[(2 * t + 1) * kHeadDim + 16 * mt + 8 + g] = o[mt][3] * i1;
-    }
-    // base-2 lse of heads 2t, 2t+1 (lane g == 0 of each column has them all)
+    // base-2 lse of heads 2t, 2t+1
     const float l0 = bad ? NAN : (e0 > 0.f ? m0 + lg2(e0) : -INFINITY);
     const float l1 = bad ? NAN : (e1 > 0.f ? m1 + lg2(e1) : -INFINITY);
-    __syncwarp();
-    // lane l moves head l/4, dims 16(l%4)..+15
-    const int hh = lane >> 2, dq = (lane & 3) * 16;
-    const float la = __shfl_sync(0xffffffffu, l0, hh >> 1);   // lane t (g = 0): heads 2t, 2t+1
-    const float lb = __shfl_sync(0xffffffffu, l1, hh >> 1);
-    const float lse_h = (hh & 1) ? lb : la;
-    const float4 *src = reinterpret_cast<const float4 *>(staging + hh * kHeadDim + dq);
-    float4 v[4] = {src[0], src[1], src[2], src[3]};
-    const size_t orow = static_cast<size_t>(cur_b) * p.num_qo_heads + head0 + hh;
+    const size_t orow0 = static_cast<size_t>(cur_b) * p.num_qo_heads + head0;
     if (whole) {
-      if (hh < nheads) {
-        uint4 packed[2];
-        const float nanv = NAN;
-        auto pk = [&](float a, float c) { return bad ? pack_bf16(nanv, nanv) : pack_bf16(a, c); };
-        packed[0] = make_uint4(pk(v[0].x, v[0].y), pk(v[0].z, v[0].w), pk(v[1].x, v[1].y), pk(v[1].z, v[1].w));
-        packed[1] = make_uint4(pk(v[2].x, v[2].y), pk(v[2].z, v[2].w), pk(v[3].x, v[3].y), pk(v[3].z, v[3].w));
-        uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * kHeadDim + dq);
-        dst[0] = packed[0];
-        dst[1] = packed[1];
-        if (p.lse && (lane & 3) == 0) p.lse[orow] = lse_h * kLn2;
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int hh = frag_head(k);
+          if (hh < nheads) {
+            const float v = bad ? NAN : o[mt][k] * ((k & 1) ? i1 : i0);
+            reinterpret_cast<__nv_bfloat16 *>(p.out)[(orow0 + hh) * kHeadDim + frag_dim(mt, k)] =
+                __float2bfloat16_rn(v);
+          }
+        }
+      if (p.lse && g == 0) {
+        if (2 * t < nheads) p.lse[orow0 + 2 * t] = l0 * kLn2;
+        if (2 * t + 1 < nheads) p.lse[orow0 + 2 * t + 1] = l1 * kLn2;
       }
     } else {
-      // chunk result -> slot (worker, first-or-last chunk of its range)
+      // chunk result in fragment order -> slot (worker, first-or-last chunk)
       const long long unit_start = prefix[cur_b] + static_cast<long long>(cur_uh) * np;
       const bool first_of_range = unit_start + chunk_first_pg == r0;
       const long long slot = 2 * w + (first_of_range ? 0 : 1);
-      float4 *dst = reinterpret_cast<float4 *>(p.ws_o + (slot * kHeadsPerTile + hh) * kHeadDim + dq);
+      float4 *dst = reinterpret_cast<float4 *>(p.ws_o + slot * kHeadsPerTile * kHeadDim + lane * 16);
       const float nanv = NAN;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) dst[k] = bad ? make_float4(nanv, nanv, nanv, nanv) : v[k];
-      if ((lane & 3) == 0) p.ws_lse[slot * kHeadsPerTile + hh] = lse_h;
-      __threadfence();
+      for (int mt = 0; mt < 4; ++mt)
+        dst[mt] = bad ? make_float4(nanv, nanv, nanv, nanv)
+                      : make_float4(o[mt][0] * i0, o[mt][1] * i1, o[mt][2] * i0, o[mt][3] * i1);
+      if (g == 0) {
+        p.ws_lse[slot * kHeadsPerTile + 2 * t] = l0;
+        p.ws_lse[slot * kHeadsPerTile + 2 * t + 1] = l1;
+      }
       __syncwarp();
       // contributors: workers whose ranges meet the unit
       const long long unit_end = unit_start + np;                 // exclusive
@@ -291,52 +303,62 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       const long long wl = (unit_end * workers - 1) / total;
       const int unit_id = cur_b * units_per_req + cur_uh;
       int last = 0;
-      if (lane == 0) last = atomicAdd(&p.counters[unit_id], 1) == static_cast<int>(wl - wf);
+      if (lane == 0) last = atomic_add_acq_rel(&p.counters[unit_id], 1) == static_cast<int>(wl - wf);
       last = __shfl_sync(0xffffffffu, last, 0);
       if (last) {
-        __threadfence();
-        // online log-sum-exp over the chunks, head hh, dims dq..dq+15
-        float mx = -INFINITY, den = 0.f;
+        // online log-sum-exp over the chunks, per lane: heads 2t, 2t+1
+        float mx[2] = {-INFINITY, -INFINITY}, den[2] = {0.f, 0.f};
         bool poisoned = false;     // a chunk reported NaN (bad page, failed wait)
-        float acc[16];
+        float acc[4][4];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+        for (int mt = 0; mt < 4; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
         for (long long c = wf; c <= wl; ++c) {
           const long long cs = 2 * c + ((c * total / workers) >= unit_start ? 0 : 1);
-          const float lc = __ldcg(p.ws_lse + cs * kHeadsPerTile + hh);
-          const float4 *src2 = reinterpret_cast<const float4 *>(p.ws_o + (cs * kHeadsPerTile + hh) * kHeadDim + dq);
-          if (lc != lc) {
-            poisoned = true;
-            continue;
+          const float lc[2] = {__ldcg(p.ws_lse + cs * kHeadsPerTile + 2 * t),
+                               __ldcg(p.ws_lse + cs * kHeadsPerTile + 2 * t + 1)};
+          const float4 *src = reinterpret_cast<const float4 *>(p.ws_o + cs * kHeadsPerTile * kHeadDim + lane * 16);
+          float a[2], wgt[2];
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            if (lc[h2] != lc[h2]) poisoned = true;
+            if (lc[h2] != lc[h2] || lc[h2] == -INFINITY) {
+              a[h2] = 1.f;
+              wgt[h2] = 0.f;
+              continue;
+            }
+            const float nm = fmaxf(mx[h2], lc[h2]);
+            a[h2] = mx[h2] == -INFINITY ? 0.f : ex2(mx[h2] - nm);
+            wgt[h2] = ex2(lc[h2] - nm);
+            den[h2] = den[h2] * a[h2] + wgt[h2];
+            mx[h2] = nm;
           }
-          if (lc == -INFINITY) continue;
-          const float nm = fmaxf(mx, lc);
-          const float a = mx == -INFINITY ? 0.f : ex2(mx - nm);
-          const float wgt = ex2(lc - nm);
-          den = den * a + wgt;
+#pragma unroll
+          for (int mt = 0; mt < 4; ++mt) {
+            const float4 q4 = __ldcg(src + mt);
+            acc[mt][0] = wgt[0] == 0.f ? acc[mt][0] : acc[mt][0] * a[0] + wgt[0] * q4.x;
+            acc[mt][1] = wgt[1] == 0.f ? acc[mt][1] : acc[mt][1] * a[1] + wgt[1] * q4.y;
+            acc[mt][2] = wgt[0] == 0.f ? acc[mt][2] : acc[mt][2] * a[0] + wgt[0] * q4.z;
+            acc[mt][3] = wgt[1] == 0.f ? acc[mt][3] : acc[mt][3] * a[1] + wgt[1] * q4.w;
+          }
+        }
+        const float inv[2] = {den[0] > 0.f ? 1.f / den[0] : 0.f, den[1] > 0.f ? 1.f / den[1] : 0.f};
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const float4 q4 = __ldcg(src2 + k);
-            acc[4 * k + 0] = acc[4 * k + 0] * a + wgt * q4.x;
-            acc[4 * k + 1] = acc[4 * k + 1] * a + wgt * q4.y;
-            acc[4 * k + 2] = acc[4 * k + 2] * a + wgt * q4.z;
-            acc[4 * k + 3] = acc[4 * k + 3] * a + wgt * q4.w;
+            const int hh = frag_head(k);
+            if (hh < nheads) {
+              const float v = poisoned ? NAN : acc[mt][k] * inv[k & 1];
+              reinterpret_cast<__nv_bfloat16 *>(p.out)[(orow0 + hh) * kHeadDim + frag_dim(mt, k)] =
+                  __float2bfloat16_rn(v);
+            }
           }
-          mx = nm;
-        }
-        if (hh < nheads) {
-          const float inv = den > 0.f ? 1.f / den : 0.f;
-          uint4 packed[2];
-          packed[0] = make_uint4(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv),
-                                 pack_bf16(acc[4] * inv, acc[5] * inv), pack_bf16(acc[6] * inv, acc[7] * inv));
-          packed[1] = make_uint4(pack_bf16(acc[8] * inv, acc[9] * inv), pack_bf16(acc[10] * inv, acc[11] * inv),
-                                 pack_bf16(acc[12] * inv, acc[13] * inv), pack_bf16(acc[14] * inv, acc[15] * inv));
-          if (poisoned) packed[0] = packed[1] = make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
-          uint4 *dst2 = reinterpret_cast<uint4 *>(p.out + orow * kHeadDim + dq);
-          dst2[0] = packed[0];
-          dst2[1] = packed[1];
-          if (p.lse && (lane & 3) == 0)
-            p.lse[orow] = poisoned ? NAN : (den > 0.f ? (mx + lg2(den)) * kLn2 : -INFINITY);
+        if (p.lse && g == 0) {
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2)
+            if (2 * t + h2 < nheads)
+              p.lse[orow0 + 2 * t + h2] =
+                  poisoned ? NAN : (den[h2] > 0.f ? (mx[h2] + lg2(den[h2])) * kLn2 : -INFINITY);
         }
         if (lane == 0) p.counters[unit_id] = 0;      // ready for the next call
       }
@@ -365,7 +387,7 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       failed = true;
     }
     const uint32_t sbase = smem_u32(stages + st * kStageBytes);
-    const uint32_t kbase = sbase, vbase = sbase + kTileBytes, qbase = sbase + 2 * kTileBytes;
+    const uint32_t kbase = sbase, vbase = sbase + kTileBytes;
     const int kvh = uh / p.head_blocks, hb = uh % p.head_blocks;
     const int nheads = min(kHeadsPerTile, p.group - hb * kHeadsPerTile);
     if (chunk_start) {
@@ -385,23 +407,19 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       }
 #pragma unroll
       for (int mt = 0; mt < 4; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-      // Q^T as the B operand: rows = heads, 16-dim k-steps
-      if (!failed) {
+      // this unit's Q (prefetched at the previous chunk start, except for
+      // the first chunk), then prefetch the next unit's
+      if (i == 0) load_q(b, uh, qb);
+      else {
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          uint32_t r[4];
-          const int c = 4 * h2 + q_mat;
-          ldsm_x4(qbase + q_row * 128 + ((c ^ q_row) << 4), r);
-          qb[2 * h2][0] = r[0];
-          qb[2 * h2][1] = r[1];
-          qb[2 * h2 + 1][0] = r[2];
-          qb[2 * h2 + 1][1] = r[3];
-        }
-        if (g >= nheads) {
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks) qb[ks][0] = qb[ks][1] = 0u;
+        for (int ks = 0; ks < 4; ++ks) {
+          qb[ks][0] = qn[ks][0];
+          qb[ks][1] = qn[ks][1];
         }
       }
+      int nb, nuh;
+      next_unit(b, uh, nb, nuh);
+      load_q(nb, nuh, qn);
     }
     cur_pg = pg;
     if (__shfl_sync(0xffffffffu, (stage_bad >> st) & 1u, 0)) chunk_bad = true;
@@ -486,7 +504,7 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
 
 }  // namespace
 
-int decode_ctas_per_sm() { return 2; }
+int decode_ctas_per_sm() { return 3; }
 
 int decode_max_batch() { return kMaxBatch; }
 
@@ -495,13 +513,13 @@ size_t decode_smem_bytes(int batch, int num_qo_heads) {
          num_qo_heads * sizeof(float);
 }
 
-cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap, const CUtensorMap &qmap,
-                          const DecodeParams &p, int grid, cudaStream_t stream) {
+cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParams &p,
+                          int grid, cudaStream_t stream) {
   const size_t smem = decode_smem_bytes(p.batch, p.num_qo_heads);
   cudaError_t err = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  decode_kernel<<<grid, kNW * 32, smem, stream>>>(kmap, vmap, qmap, p);
+  decode_kernel<<<grid, kNW * 32, smem, stream>>>(kmap, vmap, p);
   return cudaGetLastError();
 }
 

@@ -39,8 +39,8 @@ size_t decode_smem_bytes(int batch, int num_qo_heads);
 // Bytes at the start of the decode workspace that must be zero before a call.
 size_t decode_counter_bytes(int batch, int num_qo_heads, int num_kv_heads);
 
-cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap, const CUtensorMap &qmap,
-                          const DecodeParams &p, int grid, cudaStream_t stream);
+cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParams &p,
+                          int grid, cudaStream_t stream);
 
 // ---------------------------------------------------------------- prefill
 struct PrefillParams {

@@ -74,6 +74,15 @@ __device__ __forceinline__ void named_barrier_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Atomic add with acquire-release semantics at GPU scope: orders this
+// thread's (and, through a preceding warp/CTA barrier, its peers') earlier
+// writes before the add, and later reads after it.
+__device__ __forceinline__ int atomic_add_acq_rel(int *addr, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+  return old;
+}
+
 // -------------------------------------------------------------------- TMA
 // 3-D tiled bulk tensor load global -> shared, completion counted in bytes
 // on an mbarrier.  Coordinates are innermost first.

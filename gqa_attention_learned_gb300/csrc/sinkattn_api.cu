@@ -222,9 +222,6 @@ int sinkattn_decode(const void *q, const void *k_cache, const void *v_cache,
   for (int b0 = 0; b0 < batch; b0 += sa::decode_max_batch()) {
     const int nb = std::min(batch - b0, sa::decode_max_batch());
     const size_t qoff = static_cast<size_t>(b0) * num_qo_heads * kHeadDim;
-    CUtensorMap qmap;
-    if (!encode_map(&qmap, static_cast<const uint16_t *>(q) + qoff, num_qo_heads, nb, 8, 1))
-      return fail_msg("cuTensorMapEncodeTiled failed");
     sa::DecodeParams p{};
     p.q = static_cast<const uint16_t *>(q) + qoff;
     p.page_table = page_table + static_cast<size_t>(b0) * max_pages_per_seq;
@@ -245,7 +242,7 @@ int sinkattn_decode(const void *q, const void *k_cache, const void *v_cache,
     p.num_pages = num_pages;
     p.num_workers = plan.workers;
     const int st = cuda_status(
-        sa::launch_decode(kmap, vmap, qmap, p, plan.grid, static_cast<cudaStream_t>(stream)),
+        sa::launch_decode(kmap, vmap, p, plan.grid, static_cast<cudaStream_t>(stream)),
         "decode launch");
     if (st != SINKATTN_OK) return st;
   }

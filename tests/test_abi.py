@@ -46,7 +46,7 @@ def test_plan_is_host_only_and_deterministic(lib):
     b = sa.decode_plan(64, 64, 8, 4096, num_sms=152)
     assert a == b
     workers, ws = a
-    assert workers == 152 * 2 * 4            # every resident warp slot
+    assert workers == 152 * 3 * 4            # every resident warp slot
     # counters (64 x 8 units, 256-byte rounded) + 2 chunk slots per worker
     assert ws == 2048 + 2 * workers * 8 * 64 * 4 + 2 * workers * 8 * 4
     # explicit worker counts are honoured up to one page per worker
@@ -60,7 +60,7 @@ def test_plan_is_host_only_and_deterministic(lib):
 
 def test_plan_long_context_workers(lib):
     s, _ = sa.decode_plan(8, 64, 8, 131072, num_sms=152)
-    assert s == 1216
+    assert s == 1824
 
 
 def test_plan_rejects_bad_arguments(lib):
