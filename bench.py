@@ -285,7 +285,7 @@ def run_long_decode(args, rank, dev):
     nbytes = decode_bytes(lens, hq, hkv)
     args_d = [w[n].to(dev) for n in ("q", "k_cache", "v_cache", "page_table", "kv_lens", "sinks")]
     res = {}
-    for label, splits in (("auto", 0), ("512 workers (~8 chunks per KV head)", 512)):
+    for label, splits in (("auto", 0), ("8 splits", 8)):
         s, ws_bytes = sa.decode_plan(len(lens), hq, hkv, w["max_kv_len"], splits)
         ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
         out = torch.empty_like(args_d[0])
@@ -299,7 +299,7 @@ def run_long_decode(args, rank, dev):
         steps = max(20, args.steps // 50)
         secs = _time_steps(torch, step, steps, args.warmup, stream)
         _, t, gbps = aggregate(nbytes * steps, secs, dev)
-        res[label] = dict(workers=s, ms_per_step=1e3 * t / steps, value=gbps / 1e9, unit="GB/s")
+        res[label] = dict(splits=s, ms_per_step=1e3 * t / steps, value=gbps / 1e9, unit="GB/s")
     del args_d
     torch.cuda.empty_cache()
     return dict(workload="long-context split-KV decode: 64 q / 8 KV heads, batch 8, "
@@ -436,7 +436,7 @@ def gpu_arm(args):
         "config": {"workload": DECODE_WORKLOAD, "batch": 64, "num_qo_heads": 64,
                    "num_kv_heads": 8, "head_dim": 64, "page_size": 16,
                    "kv_tokens": sum(int(x) for x in d["w"]["kv_lens"]),
-                   "decode_workers": d["splits"],
+                   "num_splits": d["splits"],
                    "l2": "inputs larger than L2: two KV pool copies (2 x 671 MB) alternate"},
         "pct_of_hbm_peak": round(100 * d["gbps"] / peaks["hbm_gbs"], 2),
         "roofline": {"bound": "hbm", "achieved": round(kernel_gbps, 2),

@@ -103,7 +103,7 @@ def _want(t, name, dtype, dims=None, device=None):
 
 def decode_plan(batch, num_qo_heads, num_kv_heads, max_kv_len, num_splits=0, num_sms=0,
                 head_dim=64, page_size=16):
-    """(workers, workspace bytes) that `decode` will use (host only).  A
+    """(split count, workspace bytes) that `decode` will use (host only).  A
     workspace must be zero-filled before its first use (torch.zeros)."""
     s = _c_int(num_splits)
     w = _c_size(0)

@@ -22,25 +22,24 @@ struct DecodeParams {
   const float *sinks;           // [Hq]
   uint16_t *out;                // bf16 [B][Hq][64]
   float *lse;                   // [B][Hq] or null
-  int *counters;                // [B * Hkv * head_blocks], zero between calls
-  float *ws_o;                  // fp32 [2 * num_workers][8][64] chunk outputs
-  float *ws_lse;                // fp32 [2 * num_workers][8] chunk lse (base 2)
+  int *counters;                // [B][Hkv * head_blocks], zero between calls (splits > 1)
+  float *ws_o;                  // fp32 [splits][B][Hq][64] (splits > 1)
+  float *ws_lse;                // fp32 [splits][B][Hq]     (base-2 lse)
   float scale_log2;             // scale * log2(e)
   int max_pages_per_seq;
   int batch, num_qo_heads, num_kv_heads, group, head_blocks;
-  int num_pages, num_workers;
+  int num_pages, num_splits, pages_per_chunk;
 };
 
-// Resident decode CTAs per SM, warps per CTA, requests per launch.
+// Number of CTAs the decode kernel may keep resident per SM (for planning).
 int decode_ctas_per_sm();
-int decode_warps_per_cta();
-int decode_max_batch();
-size_t decode_smem_bytes(int batch, int num_qo_heads);
+// Largest split count.
+int decode_max_splits();
 // Bytes at the start of the decode workspace that must be zero before a call.
 size_t decode_counter_bytes(int batch, int num_qo_heads, int num_kv_heads);
 
-cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParams &p,
-                          int grid, cudaStream_t stream);
+cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap,
+                          const DecodeParams &p, cudaStream_t stream);
 
 // ---------------------------------------------------------------- prefill
 struct PrefillParams {

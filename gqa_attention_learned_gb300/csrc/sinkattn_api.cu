@@ -107,34 +107,41 @@ constexpr int kPrefillTile = 128;     // query rows per prefill CTA
 constexpr int kPrefillKvTile = 128;   // keys per prefill K/V tile
 
 struct DecodePlan {
-  int workers = 1;            // KV-parallel worker warps
-  int grid = 1;               // CTAs
-  size_t counters_bytes = 0;  // unit counters (zeroed once, reset by every call)
+  int num_splits = 1;
+  int pages_per_chunk = 1;
+  size_t counters_bytes = 0;  // merge counters (zeroed once, reset by every call)
   size_t workspace_bytes = 0;
 };
 
-constexpr int kMaxWorkers = 1 << 16;
-
-// Workers: by default every resident warp slot of the GPU; an explicit count
-// is honoured up to the number of (request, KV head, head block, page) items
-// the arguments allow, so each worker has at least one page.
+// Split count: by default enough (request, KV head, chunk) CTAs for a few
+// waves of the GPU, chunks of at least kMinPagesPerChunk pages; an explicit
+// count is honoured up to one page per chunk.
 DecodePlan plan_decode(int batch, int num_qo_heads, int num_kv_heads, int max_kv_len, int num_sms,
                        int requested) {
   DecodePlan plan;
   const int group = num_qo_heads / num_kv_heads;
-  const long long units = static_cast<long long>(std::min(batch, sa::decode_max_batch())) *
-                          num_kv_heads * ceil_div(group, 8);
-  const long long max_pages = ceil_div(max_kv_len, kPageSize);
-  const long long cap = std::max(1ll, std::min<long long>(kMaxWorkers, units * max_pages));
-  const long long slots =
-      static_cast<long long>(std::max(num_sms, 1)) * sa::decode_ctas_per_sm() * sa::decode_warps_per_cta();
-  const long long w = requested > 0 ? std::min<long long>(requested, cap) : std::min(slots, cap);
-  plan.workers = static_cast<int>(std::max(1ll, w));
-  plan.grid = ceil_div(plan.workers, sa::decode_warps_per_cta());
-  plan.counters_bytes = (static_cast<size_t>(units) * sizeof(int) + 255) & ~size_t(255);
-  const size_t slots_out = 2 * static_cast<size_t>(plan.workers) * 8;
-  plan.workspace_bytes = plan.counters_bytes + slots_out * kHeadDim * sizeof(float) +
-                         ((slots_out * sizeof(float) + 255) & ~size_t(255));
+  const int head_blocks = ceil_div(group, 8);
+  const int max_pages = std::max(1, ceil_div(max_kv_len, kPageSize));
+  int s;
+  if (requested > 0) {
+    s = requested;
+  } else {
+    const long long units = static_cast<long long>(batch) * num_kv_heads * head_blocks;
+    const long long slots = static_cast<long long>(std::max(num_sms, 1)) * sa::decode_ctas_per_sm();
+    s = static_cast<int>(std::min<long long>((kWavesTarget * slots + units - 1) / std::max(units, 1ll),
+                                             1 << 20));
+    s = std::min(s, std::max(1, max_pages / kMinPagesPerChunk));
+  }
+  s = std::max(1, std::min({s, sa::decode_max_splits(), max_pages}));
+  plan.pages_per_chunk = ceil_div(max_pages, s);
+  plan.num_splits = ceil_div(max_pages, plan.pages_per_chunk);
+  if (plan.num_splits > 1) {
+    const size_t units = static_cast<size_t>(batch) * num_kv_heads * head_blocks;
+    plan.counters_bytes = (units * sizeof(int) + 255) & ~size_t(255);
+    const size_t rows = static_cast<size_t>(plan.num_splits) * batch * num_qo_heads;
+    plan.workspace_bytes = plan.counters_bytes + rows * kHeadDim * sizeof(float) +
+                           ((rows * sizeof(float) + 255) & ~size_t(255));
+  }
   return plan;
 }
 
@@ -143,7 +150,8 @@ DecodePlan plan_decode(int batch, int num_qo_heads, int num_kv_heads, int max_kv
 namespace sa {
 size_t decode_counter_bytes(int batch, int num_qo_heads, int num_kv_heads) {
   if (batch <= 0 || num_kv_heads <= 0 || num_qo_heads <= 0) return 0;
-  return plan_decode(batch, num_qo_heads, num_kv_heads, 0, 1, 1).counters_bytes;
+  const size_t units = static_cast<size_t>(batch) * num_kv_heads * ceil_div(num_qo_heads / num_kv_heads, 8);
+  return (units * sizeof(int) + 255) & ~size_t(255);
 }
 }  // namespace sa
 
@@ -176,7 +184,7 @@ int sinkattn_decode_plan(int batch, int num_qo_heads, int num_kv_heads, int head
     if (num_sms == 0) return fail_msg("no CUDA device to plan for");
   }
   const DecodePlan plan = plan_decode(batch, num_qo_heads, num_kv_heads, max_kv_len, num_sms, *num_splits);
-  *num_splits = plan.workers;
+  *num_splits = plan.num_splits;
   *workspace_bytes = plan.workspace_bytes;
   return SINKATTN_OK;
 }
@@ -201,14 +209,16 @@ int sinkattn_decode(const void *q, const void *k_cache, const void *v_cache,
     return SINKATTN_INVALID_ARGUMENT;
   const int group = num_qo_heads / num_kv_heads;
   const int head_blocks = ceil_div(group, 8);
+  if (batch > 65535 || static_cast<long long>(num_kv_heads) * head_blocks > 65535)
+    return SINKATTN_UNSUPPORTED;
 
   const int sms = device_sm_count();
   if (sms == 0) return fail_msg("no CUDA device (SM count query failed)");
   const DecodePlan plan = plan_decode(batch, num_qo_heads, num_kv_heads, max_kv_len, sms, num_splits);
-  if (!workspace || workspace_bytes < plan.workspace_bytes) return SINKATTN_WORKSPACE_TOO_SMALL;
-  if (!aligned(workspace, 256)) return SINKATTN_INVALID_ARGUMENT;
-  if (sa::decode_smem_bytes(std::min(batch, sa::decode_max_batch()), num_qo_heads) > 227 * 1024)
-    return SINKATTN_UNSUPPORTED;
+  if (plan.num_splits > 1) {
+    if (!workspace || workspace_bytes < plan.workspace_bytes) return SINKATTN_WORKSPACE_TOO_SMALL;
+    if (!aligned(workspace, 256)) return SINKATTN_INVALID_ARGUMENT;
+  }
 
   CUtensorMap kmap, vmap;
   const unsigned long long rows = static_cast<unsigned long long>(num_kv_heads) * kPageSize;
@@ -216,37 +226,31 @@ int sinkattn_decode(const void *q, const void *k_cache, const void *v_cache,
       !encode_rows_map(&vmap, v_cache, rows, num_pages, kPageSize))
     return fail_msg("cuTensorMapEncodeTiled failed");
 
-  uint8_t *ws = static_cast<uint8_t *>(workspace);
-  // requests go in launches of at most decode_max_batch(); the workspace is
-  // reused launch after launch on the same stream
-  for (int b0 = 0; b0 < batch; b0 += sa::decode_max_batch()) {
-    const int nb = std::min(batch - b0, sa::decode_max_batch());
-    const size_t qoff = static_cast<size_t>(b0) * num_qo_heads * kHeadDim;
-    sa::DecodeParams p{};
-    p.q = static_cast<const uint16_t *>(q) + qoff;
-    p.page_table = page_table + static_cast<size_t>(b0) * max_pages_per_seq;
-    p.kv_lens = kv_lens + b0;
-    p.sinks = sinks;
-    p.out = static_cast<uint16_t *>(out) + qoff;
-    p.lse = lse ? lse + static_cast<size_t>(b0) * num_qo_heads : nullptr;
+  sa::DecodeParams p{};
+  p.q = static_cast<const uint16_t *>(q);
+  p.page_table = page_table;
+  p.kv_lens = kv_lens;
+  p.sinks = sinks;
+  p.out = static_cast<uint16_t *>(out);
+  p.lse = lse;
+  if (plan.num_splits > 1) {
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
     p.counters = reinterpret_cast<int *>(ws);
     p.ws_o = reinterpret_cast<float *>(ws + plan.counters_bytes);
-    p.ws_lse = p.ws_o + 2 * static_cast<size_t>(plan.workers) * 8 * kHeadDim;
-    p.scale_log2 = scale * sa::kLog2e;
-    p.max_pages_per_seq = max_pages_per_seq;
-    p.batch = nb;
-    p.num_qo_heads = num_qo_heads;
-    p.num_kv_heads = num_kv_heads;
-    p.group = group;
-    p.head_blocks = head_blocks;
-    p.num_pages = num_pages;
-    p.num_workers = plan.workers;
-    const int st = cuda_status(
-        sa::launch_decode(kmap, vmap, p, plan.grid, static_cast<cudaStream_t>(stream)),
-        "decode launch");
-    if (st != SINKATTN_OK) return st;
+    p.ws_lse = p.ws_o + static_cast<size_t>(plan.num_splits) * batch * num_qo_heads * kHeadDim;
   }
-  return SINKATTN_OK;
+  p.scale_log2 = scale * sa::kLog2e;
+  p.max_pages_per_seq = max_pages_per_seq;
+  p.batch = batch;
+  p.num_qo_heads = num_qo_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = group;
+  p.head_blocks = head_blocks;
+  p.num_pages = num_pages;
+  p.num_splits = plan.num_splits;
+  p.pages_per_chunk = plan.pages_per_chunk;
+  return cuda_status(sa::launch_decode(kmap, vmap, p, static_cast<cudaStream_t>(stream)),
+                     "decode launch");
 }
 
 int sinkattn_prefill(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,

@@ -76,12 +76,13 @@ SINKATTN_API const char *sinkattn_last_error(void);
 SINKATTN_API int sinkattn_version(void);
 
 /*
- * Work plan for sinkattn_decode (host only, no launch).
+ * Split plan for sinkattn_decode (host only, no launch).
  *   num_sms          : SMs to plan for; 0 = ask the current CUDA device.
- *   num_splits       : in = requested number of KV-parallel workers (0 =
- *                      every resident warp slot of the GPU), out = the number
- *                      sinkattn_decode will use (at most one per KV page).
- *   workspace_bytes  : out = bytes of workspace that decode needs.
+ *   num_splits       : in = requested number of KV chunks per (request, KV
+ *                      head) (0 = choose), out = the count sinkattn_decode
+ *                      will use (at most one page per chunk).
+ *   workspace_bytes  : out = bytes of workspace that decode needs (0 when the
+ *                      plan has a single split).
  * Same inputs give the same plan, so the plan can be made once and reused
  * (e.g. under CUDA graph capture); max_kv_len is a host-side bound, so no
  * device-to-host read is needed.
@@ -102,19 +103,18 @@ SINKATTN_API int sinkattn_decode_plan(int batch, int num_qo_heads, int num_kv_he
  *   out        : bf16 [batch][num_qo_heads][head_dim]
  *   lse        : fp32 [batch][num_qo_heads] (natural log, sink included);
  *                may be NULL
- *   max_kv_len : host-side upper bound on kv_lens (drives the plan)
- *   num_splits : 0 = choose, else the number of KV-parallel workers (see
- *                sinkattn_decode_plan)
+ *   max_kv_len : host-side upper bound on kv_lens (drives the split plan)
+ *   num_splits : 0 = choose (see sinkattn_decode_plan), else the number of
+ *                KV chunks per (request, KV head)
  *   workspace  : device scratch of workspace_bytes (>= the plan's figure),
- *                256-byte aligned, ZERO-FILLED BEFORE ITS FIRST USE; every
- *                call leaves it ready for the next (its counters return to
- *                zero), so it is zeroed once, not per call.  Calls sharing a
- *                workspace must not overlap on the GPU.
- * The (request, KV head) pages of the whole batch are dealt out evenly to
- * the workers; a (request, KV head) cut between workers is computed as KV
- * chunks -- the sink entering the chunk that holds its first page only --
- * and merged by log-sum-exp inside the same kernel by the last chunk to
- * finish.
+ *                256-byte aligned; may be NULL when the plan has a single
+ *                split.  It must be ZERO-FILLED BEFORE ITS FIRST USE; every
+ *                call leaves it ready for the next (its merge counters return
+ *                to zero), so it is zeroed once, not per call.  Calls sharing
+ *                a workspace must not overlap on the GPU.
+ * Long contexts run as num_splits KV chunks per (request, KV head), the sink
+ * entering chunk 0 only; the last chunk to finish merges them by
+ * log-sum-exp inside the same kernel.
  */
 SINKATTN_API int sinkattn_decode(const void *q, const void *k_cache, const void *v_cache,
                     const int32_t *page_table, int max_pages_per_seq,
@@ -183,7 +183,7 @@ SINKATTN_API int sinkattn_prefill_paged(const void *q, const int32_t *cu_seqlens
  *     that first call before any stream capture on the device.
  *   - Returns SINKATTN_WORKSPACE_TOO_SMALL, launching nothing, when the plan
  *     for these sizes (see sinkattn_decode_plan) needs more scratch than the
- *     array holds (only very large explicit num_splits values do).
+ *     array holds.  Passing num_splits = 1 needs no scratch at all.
  *   - All calls share the one array, and it keeps the last call's contents.
  *     Each call first clears the part that must start at zero (the merge
  *     counters, with cudaMemsetAsync on `stream`); two calls that overlap on

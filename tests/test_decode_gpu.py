@@ -73,7 +73,7 @@ def test_long_context_split_decode(splits):
         assert sa.decode_plan(8, 64, 8, w["max_kv_len"], splits)[0] == 8
     else:
         s, _ = sa.decode_plan(8, 64, 8, w["max_kv_len"])
-        assert s >= 8
+        assert 8 <= s <= 1024
     out, lse = run_decode(w, num_splits=splits)
     ro, rl = ref_decode(w)
     assert_out_close(out, ro)

@@ -52,13 +52,13 @@ def test_static_scratch_with_other_inputs_after_first_call():
 
 
 def test_static_scratch_rejects_plans_beyond_its_size():
-    # 65536 workers need ~272 MB of chunk slots: refused on the host, nothing
-    # launched
+    # 1024 requests x 64 heads x 8 splits need ~136 MB of chunk slots: refused
+    # on the host, nothing launched
     q = torch.zeros(1024, 64, 64, dtype=torch.bfloat16, device=DEV)
     kc = torch.zeros(16, 8, 16, 64, dtype=torch.bfloat16, device=DEV)
     table = torch.zeros(1024, 1, dtype=torch.int32, device=DEV)
     lens = torch.ones(1024, dtype=torch.int32, device=DEV)
     sinks = torch.zeros(64, dtype=torch.float32, device=DEV)
     with pytest.raises(sa.SinkAttnError) as e:
-        sa.decode_static_scratch(q, kc, kc, table, lens, sinks, 0.125, 4096, num_splits=65536)
+        sa.decode_static_scratch(q, kc, kc, table, lens, sinks, 0.125, 4096, num_splits=8)
     assert e.value.status == sa.WORKSPACE_TOO_SMALL
