@@ -30,13 +30,23 @@
 #include "kernels.cuh"
 #include "ptx.cuh"
 
+#include <algorithm>
 #include <cmath>
 
 namespace sa {
 namespace {
 
-constexpr int kNW = 4;          // warps per CTA
-constexpr int kStages = 4;      // pages in flight per warp
+#ifndef SA_DECODE_NW
+#define SA_DECODE_NW 8          // warps per CTA
+#endif
+#ifndef SA_DECODE_CHUNK_MAJOR
+#define SA_DECODE_CHUNK_MAJOR 0
+#endif
+#ifndef SA_DECODE_STAGES
+#define SA_DECODE_STAGES 3      // pages in flight per warp
+#endif
+constexpr int kNW = SA_DECODE_NW;
+constexpr int kStages = SA_DECODE_STAGES;
 constexpr int kTileBytes = kPageSize * kHeadDim * 2;   // 2048
 constexpr int kStageBytes = 2 * kTileBytes;            // K + V
 constexpr int kHeadsPerTile = 8;
@@ -67,10 +77,21 @@ __device__ __forceinline__ int request_chunks(int kv_len, int max_pages_per_seq,
 __global__ void __launch_bounds__(kNW * 32)
 decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
               const DecodeParams p) {
+#if SA_DECODE_CHUNK_MAJOR
+  // chunk-major order: every request's first chunk is dispatched before any
+  // second chunk, so the last wave holds the short trailing chunks
+  const int chunk = blockIdx.z;
+  const int hb = blockIdx.x % p.head_blocks;
+  const int kvh = blockIdx.x / p.head_blocks;
+  const int b = blockIdx.y;
+  const int unit_y = blockIdx.x;
+#else
   const int chunk = blockIdx.x;
   const int hb = blockIdx.y % p.head_blocks;
   const int kvh = blockIdx.y / p.head_blocks;
   const int b = blockIdx.z;
+  const int unit_y = blockIdx.y;
+#endif
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
 
@@ -330,7 +351,7 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
   __shared__ int is_last;
   __threadfence();
   __syncthreads();
-  const size_t unit = static_cast<size_t>(b) * gridDim.y + blockIdx.y;
+  const size_t unit = static_cast<size_t>(b) * (p.num_kv_heads * p.head_blocks) + unit_y;
   if (threadIdx.x == 0) is_last = atomicAdd(&p.counters[unit], 1) == nchunks - 1;
   __syncthreads();
   if (!is_last) return;
@@ -378,7 +399,10 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
 
 }  // namespace
 
-int decode_ctas_per_sm() { return 3; }
+int decode_ctas_per_sm() {
+  // shared memory bounds residency: 228 KB per SM, 1 KB of it reserved per CTA
+  return std::max(1, std::min(228 * 1024 / (kSmemBytes + 1024), 2048 / (kNW * 32)));
+}
 
 int decode_max_splits() { return 1024; }
 
@@ -388,7 +412,11 @@ cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap, cons
   cudaError_t err = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemBytes);
   if (err != cudaSuccess) return err;
+#if SA_DECODE_CHUNK_MAJOR
+  dim3 grid(p.num_kv_heads * p.head_blocks, p.batch, p.num_splits);
+#else
   dim3 grid(p.num_splits, p.num_kv_heads * p.head_blocks, p.batch);
+#endif
   decode_kernel<<<grid, kNW * 32, kSmemBytes, stream>>>(kmap, vmap, p);
   return cudaGetLastError();
 }
