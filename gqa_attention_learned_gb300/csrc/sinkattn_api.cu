@@ -20,7 +20,7 @@ using sa::kPageSize;
 
 constexpr int kMaxDevices = 64;
 constexpr int kMinPagesPerChunk = 16;   // keeps merge traffic under ~3% of KV
-constexpr int kWavesTarget = 3;
+constexpr int kWavesTarget = 4;
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
