@@ -8,18 +8,23 @@
 // sees keys j <= kv_len - q_len + i (for plain prefill kv_len = q_len).
 //
 // One CTA = one 128-row query tile of one query head (6 warps):
-//   warp 4      TMA producer: the Q tile once, then K/V tiles of 128 keys
-//               into a 2-stage ring (contiguous: one 16 KB box each; paged:
-//               eight 2 KB page boxes each), 128-byte swizzle.
+//   warp 4      TMA producer: the Q tile once, then K and V tiles of 128
+//               keys into two 2-stage rings with their own barriers
+//               (contiguous: one 16 KB box each; paged: eight 2 KB page
+//               boxes each), 128-byte swizzle.
 //   warp 5      MMA issuer (one thread): S = Q K^T (tcgen05.mma, A and B
 //               from shared memory, M=128 N=128 K=16 x4) into tensor memory;
-//               then O += P V (A = P from tensor memory, B = V from shared
-//               memory in MN-major layout, M=128 N=64 K=16 x8).
+//               O += P V (A = P from tensor memory, B = V from shared memory
+//               in MN-major layout, M=128 N=64 K=16 x8).  S of tile j+1 is
+//               issued as soon as the softmax has read S of tile j, so the
+//               tensor core computes it during that softmax, and P V of tile
+//               j runs during the softmax of tile j+1.
 //   warps 0..3  softmax, one thread per query row (= tensor-memory lane):
 //               S from tensor memory (read once per tile), online softmax in
-//               base 2 started at the sink, P (bf16) back into tensor memory;
-//               O accumulates in tensor memory across KV tiles and is
-//               rescaled only when a row max grows by more than 2^8.
+//               base 2 started at the sink, P (bf16) back into tensor memory
+//               once the previous P V has finished reading it; O
+//               accumulates in tensor memory across KV tiles and is rescaled
+//               only when a row max grows by more than 2^8.
 // Tensor memory per CTA: S 128 columns, P 64, O 64 = 256, so two CTAs share
 // an SM and their MMA and softmax phases interleave.  Heavier query tiles
 // (later ones, which see more keys) are launched first.
@@ -46,16 +51,21 @@ constexpr uint32_t kColS = 0, kColP = 128, kColO = 192;
 constexpr float kRescaleLog2 = 8.f;     // lazy O rescale threshold (P < 256)
 
 constexpr int kOffQ = 0;
-constexpr int kOffStage = kTileBytes;                       // K then V per stage
-constexpr int kOffBars = kOffStage + kStages * 2 * kTileBytes;
+constexpr int kOffK = kTileBytes;
+constexpr int kOffV = kOffK + kStages * kTileBytes;
+constexpr int kOffBars = kOffV + kStages * kTileBytes;
 constexpr int kSmemBytes = kOffBars + 256 + 1024;           // barriers + alignment slack
 
 struct Bars {
   uint64_t q_full;
-  uint64_t kv_full[kStages];
-  uint64_t kv_empty[kStages];
-  uint64_t s_full;
-  uint64_t p_full;
+  uint64_t k_full[kStages];
+  uint64_t k_empty[kStages];
+  uint64_t v_full[kStages];
+  uint64_t v_empty[kStages];
+  uint64_t s_full;     // S of the current tile is in tensor memory
+  uint64_t s_free;     // the softmax has read S (the next QK^T may overwrite it)
+  uint64_t p_full;     // P of the current tile is in tensor memory
+  uint64_t pv_done;    // the P V of the previous tile has finished (P may be rewritten)
   uint64_t o_final;
   uint32_t tmem_base;
   int bad;
@@ -168,8 +178,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                                               ~uintptr_t(1023));
   Bars &bar = *reinterpret_cast<Bars *>(smem + kOffBars);
   uint8_t *sQ = smem + kOffQ;
-  auto sK = [&](int s) { return smem + kOffStage + s * 2 * kTileBytes; };
-  auto sV = [&](int s) { return smem + kOffStage + s * 2 * kTileBytes + kTileBytes; };
+  auto sK = [&](int s) { return smem + kOffK + s * kTileBytes; };
+  auto sV = [&](int s) { return smem + kOffV + s * kTileBytes; };
 
   if (warp == kMmaWarp) {
     tmem_alloc(&bar.tmem_base, kTmemCols);
@@ -178,11 +188,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
   if (threadIdx.x == kProducerWarp * 32) {
     mbar_init(&bar.q_full, 1);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bar.kv_full[s], 1);
-      mbar_init(&bar.kv_empty[s], 1);
+      mbar_init(&bar.k_full[s], 1);
+      mbar_init(&bar.k_empty[s], 1);
+      mbar_init(&bar.v_full[s], 1);
+      mbar_init(&bar.v_empty[s], 1);
     }
     mbar_init(&bar.s_full, 1);
+    mbar_init(&bar.s_free, kBM);
     mbar_init(&bar.p_full, kBM);
+    mbar_init(&bar.pv_done, 1);
     mbar_init(&bar.o_final, 1);
     bar.bad = 0;
     fence_mbar_init();
@@ -204,34 +218,45 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const int32_t *table = kPaged ? p.page_table + static_cast<size_t>(seq) * p.max_pages_per_seq : nullptr;
     for (int j = 0; j < n_tiles; ++j) {
       const int s = j % kStages;
-      if (j >= kStages &&
-          !__all_sync(0xffffffffu, mbar_wait(&bar.kv_empty[s], ((j / kStages) + 1) & 1))) {
+      const uint32_t ph = ((j / kStages) + 1) & 1;
+      // lanes 0..7 each own one 16-token page of the 128-key tile (paged)
+      int pid = -1;
+      bool ok = false;
+      if constexpr (kPaged) {
+        const int pg = j * (kBN / kPageSize) + lane;
+        if (lane < kBN / kPageSize && pg < npages) pid = table[pg];
+        ok = pid >= 0 && pid < p.num_pages;
+        if (lane < kBN / kPageSize && pg < npages && !ok) atomicOr(&bar.bad, 1);
+      }
+      const unsigned mask = __ballot_sync(0xffffffffu, ok);
+      const int off = lane * kPageSize * kHeadDim * 2;
+      bool waited = true;
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {                  // K, then V
+        uint64_t *full = t == 0 ? &bar.k_full[s] : &bar.v_full[s];
+        uint64_t *empty = t == 0 ? &bar.k_empty[s] : &bar.v_empty[s];
+        uint8_t *dst = t == 0 ? sK(s) : sV(s);
+        const CUtensorMap *map = t == 0 ? &kmap : &vmap;
+        if (j >= kStages && !__all_sync(0xffffffffu, mbar_wait(empty, ph))) {
+          waited = false;
+          break;
+        }
+        if constexpr (kPaged) {
+          if (lane == 0) mbar_arrive_expect_tx(full, __popc(mask) * kPageSize * kHeadDim * 2);
+          __syncwarp();
+          if (ok) tma_load_3d(dst + off, map, full, 0, kvh * kPageSize, pid);
+        } else {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(full, kTileBytes);
+            tma_load_3d(dst, map, full, 0, kvh, k_start + j * kBN);
+          }
+        }
+        __syncwarp();
+      }
+      if (!waited) {
         if (lane == 0) atomicOr(&bar.bad, 1);
         break;
       }
-      if constexpr (kPaged) {
-        // lanes 0..7 each own one 16-token page of the 128-key tile
-        const int pg = j * (kBN / kPageSize) + lane;
-        int pid = -1;
-        if (lane < kBN / kPageSize && pg < npages) pid = table[pg];
-        const bool ok = pid >= 0 && pid < p.num_pages;
-        if (lane < kBN / kPageSize && pg < npages && !ok) atomicOr(&bar.bad, 1);
-        const unsigned mask = __ballot_sync(0xffffffffu, ok);
-        if (lane == 0) mbar_arrive_expect_tx(&bar.kv_full[s], __popc(mask) * 2 * kPageSize * kHeadDim * 2);
-        __syncwarp();
-        if (ok) {
-          const int off = lane * kPageSize * kHeadDim * 2;
-          tma_load_3d(sK(s) + off, &kmap, &bar.kv_full[s], 0, kvh * kPageSize, pid);
-          tma_load_3d(sV(s) + off, &vmap, &bar.kv_full[s], 0, kvh * kPageSize, pid);
-        }
-      } else {
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&bar.kv_full[s], 2 * kTileBytes);
-          tma_load_3d(sK(s), &kmap, &bar.kv_full[s], 0, kvh, k_start + j * kBN);
-          tma_load_3d(sV(s), &vmap, &bar.kv_full[s], 0, kvh, k_start + j * kBN);
-        }
-      }
-      __syncwarp();
     }
   } else if (warp == kMmaWarp) {
     // ----------------------------------------------------------------- MMA
@@ -240,7 +265,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const uint64_t dq = umma_desc_sw128(smem_u32(sQ), 16, 1024);
     auto issue_qk = [&](int j) -> bool {
       const int s = j % kStages;
-      if (!__all_sync(0xffffffffu, mbar_wait(&bar.kv_full[s], (j / kStages) & 1))) return false;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bar.k_full[s], (j / kStages) & 1))) return false;
       tc_fence_after();
       if (lane == 0) {
         const uint64_t dk = umma_desc_sw128(smem_u32(sK(s)), 16, 1024);
@@ -248,6 +273,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         for (int kk = 0; kk < kHeadDim / 16; ++kk)
           umma_ss(tS, dq + 2 * kk, dk + 2 * kk, kIdescQK, kk > 0);   // +32 bytes per k-step
         umma_commit(&bar.s_full);
+        umma_commit(&bar.k_empty[s]);
       }
       __syncwarp();
       return true;
@@ -255,7 +281,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     if (ok) ok = issue_qk(0);
     for (int j = 0; ok && j < n_tiles; ++j) {
       const int s = j % kStages;
-      if (!__all_sync(0xffffffffu, mbar_wait(&bar.p_full, j & 1))) { ok = false; break; }
+      if (j + 1 < n_tiles) {
+        // S of tile j has been read: compute S of tile j+1 during this softmax
+        if (!__all_sync(0xffffffffu, mbar_wait(&bar.s_free, j & 1))) { ok = false; break; }
+        tc_fence_after();
+        if (!issue_qk(j + 1)) { ok = false; break; }
+      }
+      if (!__all_sync(0xffffffffu, mbar_wait(&bar.p_full, j & 1)) ||
+          !__all_sync(0xffffffffu, mbar_wait(&bar.v_full[s], (j / kStages) & 1))) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       const int valid = kv_len - j * kBN;        // keys of this tile inside the request
       if (valid < kBN) {
@@ -270,10 +306,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
           umma_ts(tO, tP + 8 * kk, dv + (2048 >> 4) * kk, kIdescPV, (j > 0) || (kk > 0));  // 16 keys = 2 KB
-        umma_commit(&bar.kv_empty[s]);
+        umma_commit(&bar.v_empty[s]);
+        umma_commit(&bar.pv_done);
       }
       __syncwarp();
-      if (j + 1 < n_tiles && !issue_qk(j + 1)) { ok = false; break; }
     }
     if (!ok && lane == 0) atomicOr(&bar.bad, 1);
     if (lane == 0) umma_commit(&bar.o_final);
@@ -309,6 +345,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       reg_tie32(x[1]);
       reg_tie32(x[2]);
       reg_tie32(x[3]);
+      tc_fence_before();
+      mbar_arrive(&bar.s_free);
       const int k0 = j * kBN;
       if (__any_sync(0xffffffffu, k0 + kBN > limit)) {   // only tiles on the causal edge
 #pragma unroll
@@ -357,15 +395,20 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       for (int c = 0; c < 4; ++c) {
         acc[c] = 0;                                   // (+0.f, +0.f)
         pack_chunk(x[c], scale2, negmu2, acc[c]);     // pairs packed in place
-        tmem_st16(trow + kColP + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&x[c][0]));
       }
       float s0, s1;
       f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), s0, s1);
       d += s0 + s1;
+      // the previous tile's P V reads P and accumulates O: wait for it
+      if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(&bar.pv_done, (j - 1) & 1))) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        tmem_st16(trow + kColP + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&x[c][0]));
       tmem_st_wait();
       if (__any_sync(0xffffffffu, rescale)) {
-        // rare: scale this row's O (finished by the previous PV; the next PV
-        // is issued only after p_full below)
+        // rare: scale this row's O (the previous P V has finished, the next
+        // one is issued only after p_full below)
 #pragma unroll
         for (int h = 0; h < 2; ++h) tmem_ld32(trow + kColO + 32 * h, x[h]);
         tmem_ld_wait32(x[0]);
