@@ -8,17 +8,19 @@
 // sees keys j <= kv_len - q_len + i (for plain prefill kv_len = q_len).
 //
 // One CTA = one 128-row query tile of one query head (6 warps):
-//   warp 4      TMA producer: the Q tile once, then K and V tiles of 128
-//               keys into two 2-stage rings with their own barriers
-//               (contiguous: one 16 KB box each; paged: eight 2 KB page
-//               boxes each), 128-byte swizzle.
-//   warp 5      MMA issuer (one thread): S = Q K^T (tcgen05.mma, A and B
-//               from shared memory, M=128 N=128 K=16 x4) into tensor memory;
+//   warp 4      loads Q once and K tiles of 128 keys into a 3-stage ring
+//               (contiguous: one 16 KB box per tile; paged: eight 2 KB page
+//               boxes), 128-byte swizzle; one thread issues S = Q K^T
+//               (tcgen05.mma, A and B from shared memory, M=128 N=128 K=16
+//               x4) into tensor memory as soon as the softmax has read the
+//               previous S, so S of tile j+1 is computed during the softmax
+//               of tile j.
+//   warp 5      loads V tiles into a 2-stage ring; one thread issues
 //               O += P V (A = P from tensor memory, B = V from shared memory
-//               in MN-major layout, M=128 N=64 K=16 x8).  S of tile j+1 is
-//               issued as soon as the softmax has read S of tile j, so the
-//               tensor core computes it during that softmax, and P V of tile
-//               j runs during the softmax of tile j+1.
+//               in MN-major layout, M=128 N=64 K=16 x8), which runs during
+//               the softmax of the next tile.  An issuing thread stalls while
+//               the tensor pipe is busy, so QK^T and P V have a thread each
+//               and S never waits behind P V.
 //   warps 0..3  softmax, one thread per query row (= tensor-memory lane):
 //               S from tensor memory (read once per tile), online softmax in
 //               base 2 started at the sink, P (bf16) back into tensor memory
@@ -42,7 +44,7 @@ namespace {
 
 constexpr int kBM = 128;                       // query rows per CTA
 constexpr int kBN = 128;                       // keys per KV tile
-constexpr int kStages = 2;
+constexpr int kKStages = 3, kVStages = 2;   // K is needed a softmax earlier than V
 constexpr int kTileBytes = kBN * kHeadDim * 2;    // 16 KB
 constexpr int kThreads = 192;
 constexpr int kProducerWarp = 4, kMmaWarp = 5;
@@ -52,16 +54,16 @@ constexpr float kRescaleLog2 = 8.f;     // lazy O rescale threshold (P < 256)
 
 constexpr int kOffQ = 0;
 constexpr int kOffK = kTileBytes;
-constexpr int kOffV = kOffK + kStages * kTileBytes;
-constexpr int kOffBars = kOffV + kStages * kTileBytes;
+constexpr int kOffV = kOffK + kKStages * kTileBytes;
+constexpr int kOffBars = kOffV + kVStages * kTileBytes;
 constexpr int kSmemBytes = kOffBars + 256 + 1024;           // barriers + alignment slack
 
 struct Bars {
   uint64_t q_full;
-  uint64_t k_full[kStages];
-  uint64_t k_empty[kStages];
-  uint64_t v_full[kStages];
-  uint64_t v_empty[kStages];
+  uint64_t k_full[kKStages];
+  uint64_t k_empty[kKStages];
+  uint64_t v_full[kVStages];
+  uint64_t v_empty[kVStages];
   uint64_t s_full;     // S of the current tile is in tensor memory
   uint64_t s_free;     // the softmax has read S (the next QK^T may overwrite it)
   uint64_t p_full;     // P of the current tile is in tensor memory
@@ -187,9 +189,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
   }
   if (threadIdx.x == kProducerWarp * 32) {
     mbar_init(&bar.q_full, 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       mbar_init(&bar.k_full[s], 1);
       mbar_init(&bar.k_empty[s], 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
       mbar_init(&bar.v_full[s], 1);
       mbar_init(&bar.v_empty[s], 1);
     }
@@ -206,8 +210,39 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
   tc_fence_after();
   const uint32_t tmem = bar.tmem_base;
 
+  const int32_t *table = kPaged ? p.page_table + static_cast<size_t>(seq) * p.max_pages_per_seq : nullptr;
+  // K (t = 0) or V (t = 1) of tile j into its ring slot, once the slot is free
+  auto load = [&](int j, int t) -> bool {
+    const int ns = t == 0 ? kKStages : kVStages;
+    const int s = j % ns;
+    uint64_t *full = t == 0 ? &bar.k_full[s] : &bar.v_full[s];
+    uint64_t *empty = t == 0 ? &bar.k_empty[s] : &bar.v_empty[s];
+    uint8_t *dst = t == 0 ? sK(s) : sV(s);
+    const CUtensorMap *map = t == 0 ? &kmap : &vmap;
+    if (j >= ns && !__all_sync(0xffffffffu, mbar_wait(empty, ((j / ns) + 1) & 1)))
+      return false;
+    if constexpr (kPaged) {
+      // lanes 0..7 each own one 16-token page of the 128-key tile
+      const int pg = j * (kBN / kPageSize) + lane;
+      int pid = -1;
+      if (lane < kBN / kPageSize && pg < npages) pid = table[pg];
+      const bool ok = pid >= 0 && pid < p.num_pages;
+      if (t == 0 && lane < kBN / kPageSize && pg < npages && !ok) atomicOr(&bar.bad, 1);
+      const unsigned mask = __ballot_sync(0xffffffffu, ok);
+      if (lane == 0) mbar_arrive_expect_tx(full, __popc(mask) * kPageSize * kHeadDim * 2);
+      __syncwarp();
+      if (ok) tma_load_3d(dst + lane * kPageSize * kHeadDim * 2, map, full, 0, kvh * kPageSize, pid);
+    } else {
+      if (lane == 0) {
+        mbar_arrive_expect_tx(full, kTileBytes);
+        tma_load_3d(dst, map, full, 0, kvh, k_start + j * kBN);
+      }
+    }
+    __syncwarp();
+    return true;
+  };
   if (warp == kProducerWarp) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------- loads and QK^T (one thread)
     if (lane == 0) {
       tma_prefetch_desc(&qmap);
       tma_prefetch_desc(&kmap);
@@ -215,57 +250,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       mbar_arrive_expect_tx(&bar.q_full, kBM * kHeadDim * 2);
       tma_load_3d(sQ, &qmap, &bar.q_full, 0, head, q_start + i0);
     }
-    const int32_t *table = kPaged ? p.page_table + static_cast<size_t>(seq) * p.max_pages_per_seq : nullptr;
-    for (int j = 0; j < n_tiles; ++j) {
-      const int s = j % kStages;
-      const uint32_t ph = ((j / kStages) + 1) & 1;
-      // lanes 0..7 each own one 16-token page of the 128-key tile (paged)
-      int pid = -1;
-      bool ok = false;
-      if constexpr (kPaged) {
-        const int pg = j * (kBN / kPageSize) + lane;
-        if (lane < kBN / kPageSize && pg < npages) pid = table[pg];
-        ok = pid >= 0 && pid < p.num_pages;
-        if (lane < kBN / kPageSize && pg < npages && !ok) atomicOr(&bar.bad, 1);
-      }
-      const unsigned mask = __ballot_sync(0xffffffffu, ok);
-      const int off = lane * kPageSize * kHeadDim * 2;
-      bool waited = true;
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {                  // K, then V
-        uint64_t *full = t == 0 ? &bar.k_full[s] : &bar.v_full[s];
-        uint64_t *empty = t == 0 ? &bar.k_empty[s] : &bar.v_empty[s];
-        uint8_t *dst = t == 0 ? sK(s) : sV(s);
-        const CUtensorMap *map = t == 0 ? &kmap : &vmap;
-        if (j >= kStages && !__all_sync(0xffffffffu, mbar_wait(empty, ph))) {
-          waited = false;
-          break;
-        }
-        if constexpr (kPaged) {
-          if (lane == 0) mbar_arrive_expect_tx(full, __popc(mask) * kPageSize * kHeadDim * 2);
-          __syncwarp();
-          if (ok) tma_load_3d(dst + off, map, full, 0, kvh * kPageSize, pid);
-        } else {
-          if (lane == 0) {
-            mbar_arrive_expect_tx(full, kTileBytes);
-            tma_load_3d(dst, map, full, 0, kvh, k_start + j * kBN);
-          }
-        }
-        __syncwarp();
-      }
-      if (!waited) {
-        if (lane == 0) atomicOr(&bar.bad, 1);
-        break;
-      }
-    }
-  } else if (warp == kMmaWarp) {
-    // ----------------------------------------------------------------- MMA
-    const uint32_t tS = tmem + kColS, tP = tmem + kColP, tO = tmem + kColO;
-    bool ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_full, 0));
+    const uint32_t tS = tmem + kColS;
     const uint64_t dq = umma_desc_sw128(smem_u32(sQ), 16, 1024);
     auto issue_qk = [&](int j) -> bool {
-      const int s = j % kStages;
-      if (!__all_sync(0xffffffffu, mbar_wait(&bar.k_full[s], (j / kStages) & 1))) return false;
+      const int s = j % kKStages;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bar.k_full[s], (j / kKStages) & 1))) return false;
       tc_fence_after();
       if (lane == 0) {
         const uint64_t dk = umma_desc_sw128(smem_u32(sK(s)), 16, 1024);
@@ -278,17 +267,26 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       __syncwarp();
       return true;
     };
-    if (ok) ok = issue_qk(0);
+    bool ok = true;
+    for (int j = 0; ok && j < min(n_tiles, kKStages); ++j) ok = load(j, 0);
+    ok = ok && __all_sync(0xffffffffu, mbar_wait(&bar.q_full, 0)) && issue_qk(0);
+    for (int j = 0; ok && j + 1 < n_tiles; ++j) {
+      // S of tile j has been read: compute S of tile j+1 during this softmax
+      if (!__all_sync(0xffffffffu, mbar_wait(&bar.s_free, j & 1))) { ok = false; break; }
+      tc_fence_after();
+      ok = issue_qk(j + 1) &&
+           (j + kKStages >= n_tiles || load(j + kKStages, 0));    // K slot freed by QK^T of tile j
+    }
+    if (!ok && lane == 0) atomicOr(&bar.bad, 1);
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------- P V (one thread)
+    const uint32_t tP = tmem + kColP, tO = tmem + kColO;
+    bool ok = true;
+    for (int j = 0; ok && j < min(n_tiles, kVStages); ++j) ok = load(j, 1);
     for (int j = 0; ok && j < n_tiles; ++j) {
-      const int s = j % kStages;
-      if (j + 1 < n_tiles) {
-        // S of tile j has been read: compute S of tile j+1 during this softmax
-        if (!__all_sync(0xffffffffu, mbar_wait(&bar.s_free, j & 1))) { ok = false; break; }
-        tc_fence_after();
-        if (!issue_qk(j + 1)) { ok = false; break; }
-      }
+      const int s = j % kVStages;
       if (!__all_sync(0xffffffffu, mbar_wait(&bar.p_full, j & 1)) ||
-          !__all_sync(0xffffffffu, mbar_wait(&bar.v_full[s], (j / kStages) & 1))) {
+          !__all_sync(0xffffffffu, mbar_wait(&bar.v_full[s], (j / kVStages) & 1))) {
         ok = false;
         break;
       }
@@ -310,6 +308,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         umma_commit(&bar.pv_done);
       }
       __syncwarp();
+      // V of tile j+2 into the slot this P V reads, once it has finished
+      if (j + kVStages < n_tiles && !load(j + kVStages, 1)) { ok = false; break; }
     }
     if (!ok && lane == 0) atomicOr(&bar.bad, 1);
     if (lane == 0) umma_commit(&bar.o_final);
