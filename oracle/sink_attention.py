@@ -215,6 +215,52 @@ def prefill_paged(q, cu_seqlens_q, k_cache, v_cache, page_table, kv_lens, sinks,
     return out, lse
 
 
+def verify(q, k_cache, v_cache, page_table, kv_lens, sinks, scale, tree_mask=None):
+    """Verification of draft tokens: the q_len newest tokens of every request.
+
+    "Accelerating Sonar through speculation" (Perplexity blog): sections
+    "Target-Draft" and "MTP" run the target over the k + 1 newest tokens of a
+    request at once (bottom-right causal); section "EAGLE" verifies a tree of
+    drafts, which needs a custom mask.  Here the mask covers the draft tokens
+    only: query i of request b sees every key j < kv_len - q_len, and draft key
+    kv_len - q_len + u when u <= i (tree_mask None) or when bit u of
+    tree_mask[b][i] is set.
+
+    Written as a gather: each row's visible keys are collected explicitly and
+    handed to the definition above.
+    q: [B, q_len, Hq, D]; tree_mask: None or [B, q_len] integers (uint64 bit
+    patterns; negative int64 values are read modulo 2**64).
+    Returns out [B, q_len, Hq, D], lse [B, q_len, Hq].
+    """
+    q, sinks = _f64(q), _check_sinks(sinks)
+    batch, q_len, hq, d = q.shape
+    hkv, page_size = k_cache.shape[1], k_cache.shape[2]
+    out = np.zeros((batch, q_len, hq, d))
+    lse = np.zeros((batch, q_len, hq))
+    for b in range(batch):
+        kv_len = int(kv_lens[b])
+        prefix = kv_len - q_len
+        if prefix < 0:
+            raise ValueError("a request cannot have more new queries than keys")
+        for kvh in range(hkv):
+            k_all = gather_paged_kv(k_cache, page_table[b], kv_len, kvh, page_size)
+            v_all = gather_paged_kv(v_cache, page_table[b], kv_len, kvh, page_size)
+            for i in range(q_len):
+                if tree_mask is None:
+                    seen = [u for u in range(q_len) if u <= i]
+                else:
+                    bits = int(tree_mask[b][i]) % (1 << 64)
+                    seen = [u for u in range(q_len) if (bits >> u) & 1]
+                keys = np.concatenate([np.arange(prefix), prefix + np.array(seen, dtype=np.int64)])
+                k, v = k_all[keys], v_all[keys]
+                for h in range(hq):
+                    if kv_head_of(h, hq, hkv) != kvh:
+                        continue
+                    o, l = sink_attention(q[b, i, h][None], k, v, sinks[h], scale, [len(keys)])
+                    out[b, i, h], lse[b, i, h] = o[0], l[0]
+    return out, lse
+
+
 # --------------------------------------------------------------------------
 # The pages' own algorithm: the online softmax, one key at a time, over KV
 # blocks, with the sink only in the first block, then a log-sum-exp merge.

@@ -34,8 +34,8 @@ GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_examples.json")
 def _num(x):
     if isinstance(x, (int, float)):
         return float(x)
-    table = {"ln2": math.log(2), "ln3": math.log(3), "ln4": math.log(4), "ln6": math.log(6),
-             "ln8": math.log(8), "-inf": -math.inf, "0": 0.0, "1": 1.0}
+    table = {"ln2": math.log(2), "ln3": math.log(3), "ln4": math.log(4), "ln5": math.log(5),
+             "ln6": math.log(6), "ln8": math.log(8), "-inf": -math.inf, "0": 0.0, "1": 1.0}
     if x in table:
         return table[x]
     num, den = x.split("/")
