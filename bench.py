@@ -63,6 +63,20 @@ def decode_bytes(kv_lens, num_qo_heads, num_kv_heads, head_dim=HEAD_DIM, page_si
             + b * 4 + pages * 4)                           # kv_lens, table
 
 
+def verify_bytes(kv_lens, q_len, num_qo_heads, num_kv_heads, tree, head_dim=HEAD_DIM,
+                 page_size=16):
+    """Algorithmic bytes of one verification pass: every K and V row once,
+    q_len query/output rows and lse per request, sinks, kv_lens, the table
+    entries in use and the tree masks."""
+    kv = sum(int(n) for n in kv_lens)
+    pages = sum((int(n) + page_size - 1) // page_size for n in kv_lens)
+    b = len(kv_lens)
+    return (kv * num_kv_heads * head_dim * 2 * 2
+            + 2 * b * q_len * num_qo_heads * head_dim * 2
+            + b * q_len * num_qo_heads * 4 + num_qo_heads * 4
+            + b * 4 + pages * 4 + (b * q_len * 8 if tree else 0))
+
+
 def prefill_flops(seqlens, num_qo_heads, head_dim=HEAD_DIM):
     """QK^T and PV over the causal (lower-triangular incl. diagonal) pairs."""
     return sum(4 * head_dim * num_qo_heads * n * (n + 1) // 2 for n in seqlens)
@@ -307,6 +321,50 @@ def run_long_decode(args, rank, dev):
                 kv_bytes=nbytes, runs=res)
 
 
+def run_verify(args, rank, dev, peaks):
+    import torch
+
+    import gqa_attention_learned_gb300 as sa
+    from gqa_attention_learned_gb300 import workloads
+
+    res = {}
+    for label, q_len, tree in (("mtp 2 tokens", 2, False), ("4 tokens causal", 4, False),
+                               ("8-node tree", 8, True)):
+        w = workloads.verify_batch(seed=5 + 1000 * rank, q_len=q_len, tree=tree)
+        hq, hkv = w["num_qo_heads"], w["num_kv_heads"]
+        lens = [int(x) for x in w["kv_lens"]]
+        nbytes = verify_bytes(lens, q_len, hq, hkv, tree)
+        q = w["q"].to(dev)
+        pools = [(w["k_cache"].to(dev), w["v_cache"].to(dev))]
+        pools.append((pools[0][0].clone(), pools[0][1].clone()))
+        table, kv_lens, sinks = w["page_table"].to(dev), w["kv_lens"].to(dev), w["sinks"].to(dev)
+        mask = None if w["tree_mask"] is None else w["tree_mask"].to(dev)
+        splits, ws_bytes = sa.verify_plan(len(lens), q_len, hq, hkv, w["max_kv_len"])
+        ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+        out = torch.empty_like(q)
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+        stream = torch.cuda.current_stream()
+
+        def step(i, q=q, pools=pools, table=table, kv_lens=kv_lens, sinks=sinks, mask=mask,
+                 w=w, out=out, lse=lse, ws=ws):
+            kc, vc = pools[i & 1]
+            sa.verify(q, kc, vc, table, kv_lens, sinks, w["scale"], w["max_kv_len"],
+                      tree_mask=mask, out=out, lse=lse, workspace=ws, stream=stream)
+
+        steps = max(50, args.steps // 20)
+        secs = _time_steps(torch, step, steps, args.warmup, stream)
+        _, t, bps = aggregate(nbytes * steps, secs, dev)
+        res[label] = dict(q_len=q_len, tree=tree, splits=splits, bytes_per_step=nbytes,
+                          ms_per_step=1e3 * t / steps, value=round(bps / 1e9, 2), unit="GB/s",
+                          frac_of_hbm=round(bps / 1e9 / peaks["hbm_gbs"], 4))
+        del pools, q
+        torch.cuda.empty_cache()
+    return dict(workload="draft-token verification on the gpt-oss-20b decode batch: 64 requests, "
+                         "kv_len U[q_len,4096], 64 q / 8 KV heads, bf16 paged KV; two KV pool "
+                         "copies alternate (inputs larger than L2)",
+                kernel="decode_kernel<2, true> (rows = tokens x heads of a KV head)", runs=res)
+
+
 def run_prefill(args, rank, dev, peaks):
     import torch
 
@@ -424,6 +482,8 @@ def gpu_arm(args):
     if not args.quick:
         if "long" in sections:
             extra["long_decode"] = run_long_decode(args, rank, dev)
+        if "verify" in sections:
+            extra["verify"] = run_verify(args, rank, dev, peaks)
         if "prefill" in sections:
             extra["prefill"] = run_prefill(args, rank, dev, peaks)
         if "mixed" in sections:
@@ -571,7 +631,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--splits", type=int, default=0, help="decode split count (0 = planned)")
     ap.add_argument("--quick", action="store_true", help="headline decode only")
-    ap.add_argument("--sections", default="long,prefill,mixed",
+    ap.add_argument("--sections", default="long,verify,prefill,mixed",
                     help="extra sections after the headline decode")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

@@ -28,6 +28,11 @@ SIGNATURES = {
     "sinkattn_decode": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _vp, _c_float, _vp, _vp,
                                  _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                  _vp, _c_size, _vp]),
+    "sinkattn_verify_plan": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                      _c_int, ctypes.POINTER(_c_int), ctypes.POINTER(_c_size)]),
+    "sinkattn_verify": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _vp, _vp, _c_float, _vp, _vp,
+                                 _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                 _c_int, _vp, _c_size, _vp]),
     "sinkattn_prefill": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _vp, _c_float, _vp,
                                   _vp, _c_int, _c_int, _c_int, _vp]),
     "sinkattn_prefill_paged": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _vp, _c_int,
@@ -39,6 +44,7 @@ SIGNATURES = {
 }
 
 STATIC_SCRATCH_BYTES = 16 << 20
+MAX_VERIFY_TOKENS = 64
 
 _lib = None
 
@@ -145,6 +151,56 @@ def decode(q, k_cache, v_cache, page_table, kv_lens, sinks, scale, max_kv_len, *
             _ptr(kv_lens), _ptr(sinks), float(scale), _ptr(out), _ptr(lse), batch, hq, hkv, d,
             page, num_pages, int(max_kv_len), int(num_splits), _ptr(workspace), ws_len,
             _stream(stream)))
+    return out, lse
+
+
+def verify_plan(batch, q_len, num_qo_heads, num_kv_heads, max_kv_len, num_splits=0, num_sms=0,
+                head_dim=64, page_size=16):
+    """(split count, workspace bytes) that `verify` will use (host only)."""
+    s = _c_int(num_splits)
+    w = _c_size(0)
+    _check("sinkattn_verify_plan",
+           load().sinkattn_verify_plan(batch, q_len, num_qo_heads, num_kv_heads, head_dim,
+                                       page_size, max_kv_len, num_sms, ctypes.byref(s),
+                                       ctypes.byref(w)))
+    return s.value, w.value
+
+
+def verify(q, k_cache, v_cache, page_table, kv_lens, sinks, scale, max_kv_len, *, tree_mask=None,
+           out=None, lse=None, num_splits=0, workspace=None, stream=None, want_lse=True):
+    """Verification of the q_len newest tokens of every request (speculative
+    decoding).  q [B, q_len, Hq, 64] bf16; the tokens are the last q_len keys
+    of each request's paged KV.  tree_mask: None (causal) or int64
+    [B, q_len] holding the uint64 bit masks (bit u of row i: token i sees
+    draft token u).  Returns (out [B, q_len, Hq, 64], lse [B, q_len, Hq])."""
+    dev = q.device
+    _want(q, "q", torch.bfloat16, 4)
+    _want(k_cache, "k_cache", torch.bfloat16, 4, dev)
+    _want(v_cache, "v_cache", torch.bfloat16, 4, dev)
+    _want(page_table, "page_table", torch.int32, 2, dev)
+    _want(kv_lens, "kv_lens", torch.int32, 1, dev)
+    _want(sinks, "sinks", torch.float32, 1, dev)
+    batch, q_len, hq, d = q.shape
+    if tree_mask is not None:
+        _want(tree_mask, "tree_mask", torch.int64, 2, dev)
+        if tuple(tree_mask.shape) != (batch, q_len):
+            raise ValueError("tree_mask must be [batch, q_len]")
+    num_pages, hkv, page, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty(batch, q_len, hq, dtype=torch.float32, device=dev)
+    splits, ws_bytes = verify_plan(batch, q_len, hq, hkv, max_kv_len, num_splits, head_dim=d,
+                                   page_size=page) if batch else (1, 0)
+    if workspace is None and ws_bytes:
+        workspace = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    with torch.cuda.device(dev):
+        _check("sinkattn_verify", load().sinkattn_verify(
+            _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table), page_table.shape[1],
+            _ptr(kv_lens), _ptr(tree_mask), _ptr(sinks), float(scale), _ptr(out), _ptr(lse), batch,
+            q_len, hq, hkv, d, page, num_pages, int(max_kv_len), int(num_splits), _ptr(workspace),
+            ws_len, _stream(stream)))
     return out, lse
 
 

@@ -51,30 +51,49 @@ constexpr int kTileBytes = kPageSize * kHeadDim * 2;   // 2048
 constexpr int kStageBytes = 2 * kTileBytes;            // K + V
 constexpr int kHeadsPerTile = 8;
 
+template <int NB>
 struct __align__(16) MergeSmem {
-  float o[kNW][kHeadsPerTile][kHeadDim];
-  float m[kNW][kHeadsPerTile];
-  float d[kNW][kHeadsPerTile];
+  float o[kNW][kHeadsPerTile * NB][kHeadDim];
+  float m[kNW][kHeadsPerTile * NB];
+  float d[kNW][kHeadsPerTile * NB];
 };
 
 constexpr int kPipeBytes = kNW * kStages * kStageBytes;
 constexpr int kBarOffset = kPipeBytes;
 constexpr int kSmemBytes = kBarOffset + kNW * kStages * 8 + 1024;  // + alignment slack
-static_assert(sizeof(MergeSmem) <= kPipeBytes, "merge scratch aliases the stages");
+static_assert(sizeof(MergeSmem<2>) <= kPipeBytes, "merge scratch aliases the stages");
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 // Chunk count of one request under the plan; 0 marks a request whose
 // arguments are out of range (its outputs become NaN).
-__device__ __forceinline__ int request_chunks(int kv_len, int max_pages_per_seq, int num_splits,
-                                              int pages_per_chunk) {
-  if (kv_len < 0) return 0;
+__device__ __forceinline__ int request_chunks(int kv_len, int min_len, int max_pages_per_seq,
+                                              int num_splits, int pages_per_chunk) {
+  if (kv_len < min_len) return 0;
   const int npages = ceil_div(kv_len, kPageSize);
   if (npages > max_pages_per_seq || npages > num_splits * pages_per_chunk) return 0;
   return npages == 0 ? 1 : ceil_div(npages, pages_per_chunk);
 }
 
-__global__ void __launch_bounds__(kNW * 32)
+// Query row r of KV head kvh -> index of its [.., Hq] row in q/out/lse
+// (-1 past the last row) and its head.  Plain decode has one token per
+// request, so row r is head kvh * group + r.
+template <bool kVerify>
+__device__ __forceinline__ long long row_index(const DecodeParams &p, int b, int kvh, int r,
+                                               int &head) {
+  if constexpr (!kVerify) {
+    head = kvh * p.group + r;
+    return r < p.group ? static_cast<long long>(b) * p.num_qo_heads + head : -1;
+  } else {
+    const int tq = r / p.group;
+    head = kvh * p.group + (r - tq * p.group);
+    if (r >= p.rows) return -1;
+    return (static_cast<long long>(b) * p.q_len + tq) * p.num_qo_heads + head;
+  }
+}
+
+template <int NB, bool kVerify>
+__global__ void __launch_bounds__(kNW * 32, 2)
 decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
               const DecodeParams p) {
 #if SA_DECODE_CHUNK_MAJOR
@@ -94,9 +113,12 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
 #endif
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
+  constexpr int kCols = kHeadsPerTile * NB;       // query rows of this CTA
 
   const int kv_len = p.kv_lens[b];
-  const int nchunks = request_chunks(kv_len, p.max_pages_per_seq, p.num_splits, p.pages_per_chunk);
+  // verification needs its q_len tokens among the keys; plain decode allows kv_len = 0
+  const int nchunks = request_chunks(kv_len, kVerify ? p.q_len : 0, p.max_pages_per_seq,
+                                     p.num_splits, p.pages_per_chunk);
   bool bad = nchunks == 0;
   if (!bad && chunk >= nchunks) return;        // uniform over the CTA
   if (bad && chunk != 0) return;
@@ -107,14 +129,16 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kBarOffset) + warp * kStages;
   uint8_t *stages = smem + warp * kStages * kStageBytes;
 
-  const int head0 = kvh * p.group + hb * kHeadsPerTile;
-  const int nheads = min(kHeadsPerTile, p.group - hb * kHeadsPerTile);
+  const int row0 = hb * kCols;                  // first query row of this CTA
   const int npages = bad ? 0 : ceil_div(kv_len, kPageSize);
   const int p_begin = chunk * p.pages_per_chunk;
   const int p_end = min(npages, p_begin + p.pages_per_chunk);
   const int first = p_begin + warp;
   const int n_my = p_end > first ? ceil_div(p_end - first, kNW) : 0;
   const int32_t *table = p.page_table + static_cast<size_t>(b) * p.max_pages_per_seq;
+  // keys [0, kv_len - q_len) are visible to every row; key kv_len - q_len + u
+  // (draft token u) to the rows whose visibility mask has bit u
+  const int draft0 = kv_len - p.q_len;
 
   if (lane == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
@@ -126,34 +150,53 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
   }
   __syncwarp();
 
-  // Q^T as the B operand: lane (g, t) holds head g, dims 16ks+2t.. and 16ks+8+2t..
-  uint32_t qb[4][2];
-  {
-    const bool live = g < nheads;
-    const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
-        p.q + (static_cast<size_t>(b) * p.num_qo_heads + head0 + (live ? g : 0)) * kHeadDim);
+  // Q^T as the B operand: lane (g, t) holds row g of each column block, dims
+  // 16ks+2t.. and 16ks+8+2t..
+  uint32_t qb[NB][4][2];
+#pragma unroll
+  for (int nb = 0; nb < NB; ++nb) {
+    int head;
+    const long long ri = row_index<kVerify>(p, b, kvh, row0 + nb * kHeadsPerTile + g, head);
+    const bool live = ri >= 0;
+    const uint32_t *qrow = reinterpret_cast<const uint32_t *>(p.q + (live ? ri : 0) * kHeadDim);
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {
-      qb[ks][0] = live ? __ldg(qrow + 8 * ks + t) : 0u;
-      qb[ks][1] = live ? __ldg(qrow + 8 * ks + 4 + t) : 0u;
+      qb[nb][ks][0] = live ? __ldg(qrow + 8 * ks + t) : 0u;
+      qb[nb][ks][1] = live ? __ldg(qrow + 8 * ks + 4 + t) : 0u;
     }
   }
 
-  // Softmax state for heads 2t and 2t+1 (identical across the 8 g-lanes).
-  float m0 = -INFINITY, m1 = -INFINITY, d0 = 0.f, d1 = 0.f;
-  if (chunk == 0 && warp == 0) {
-    const float s0 = (2 * t < nheads) ? p.sinks[head0 + 2 * t] * kLog2e : -INFINITY;
-    const float s1 = (2 * t + 1 < nheads) ? p.sinks[head0 + 2 * t + 1] * kLog2e : -INFINITY;
-    m0 = s0;
-    m1 = s1;
-    if (g == 0) {            // the sink's e^(sink - m) = 1 counted once
-      d0 = 1.f;
-      d1 = 1.f;
-    }
-  }
-  float o[4][4];
+  // Softmax state of columns 2t and 2t+1 of each block (identical across the
+  // 8 g-lanes); vis: draft-token visibility of those columns.
+  float m[NB][2], d[NB][2];
+  uint64_t vis[NB][2];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      int head;
+      const int r = row0 + nb * kHeadsPerTile + 2 * t + e;
+      const long long ri = row_index<kVerify>(p, b, kvh, r, head);
+      m[nb][e] = -INFINITY;
+      d[nb][e] = 0.f;
+      vis[nb][e] = 0;
+      if (chunk == 0 && warp == 0 && ri >= 0) {
+        m[nb][e] = p.sinks[head] * kLog2e;
+        if (g == 0) d[nb][e] = 1.f;          // the sink's e^(sink - m) = 1 counted once
+      }
+      if constexpr (kVerify) {
+        if (ri >= 0) {
+          const int tq = r / p.group;
+          const uint64_t causal = tq >= 63 ? ~0ull : ((2ull << tq) - 1);
+          vis[nb][e] = p.tree_mask ? p.tree_mask[static_cast<size_t>(b) * p.q_len + tq] : causal;
+        }
+      }
+    }
+  float o[NB][4][4];
+#pragma unroll
+  for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[nb][i][0] = o[nb][i][1] = o[nb][i][2] = o[nb][i][3] = 0.f;
 
   // Page ids of this warp's pages, 32 at a time (lane j holds page j of the batch).
   auto load_ids = [&](int base) -> int {
@@ -207,49 +250,76 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
     const uint32_t kbase = smem_u32(stages + st * kStageBytes);
     const uint32_t vbase = kbase + kTileBytes;
 
-    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    float s[NB][4];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) s[nb][0] = s[nb][1] = s[nb][2] = s[nb][3] = 0.f;
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {
       uint32_t a[4];
       const int c = 2 * ks + k_hi;
       ldsm_x4(kbase + k_row * 128 + ((c ^ (k_row & 7)) << 4), a);
-      mma_bf16_16816(s, a, qb[ks][0], qb[ks][1]);
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) mma_bf16_16816(s[nb], a, qb[nb][ks][0], qb[nb][ks][1]);
     }
 
     const int tok0 = (first + i * kNW) * kPageSize;
     const bool partial = tok0 + kPageSize > kv_len;
-    // s[0]: token g / head 2t, s[1]: token g / head 2t+1, s[2], s[3]: token g+8.
+    // s[.][0]: token g / column 2t, [1]: token g / column 2t+1, [2], [3]: token g+8.
 #pragma unroll
-    for (int r = 0; r < 4; ++r) s[r] *= p.scale_log2;
+    for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) s[nb][r] *= p.scale_log2;
     if (partial) {
-      if (tok0 + g >= kv_len) s[0] = s[1] = -INFINITY;
-      if (tok0 + g + 8 >= kv_len) s[2] = s[3] = -INFINITY;
-    }
-    float x0 = fmaxf(s[0], s[2]), x1 = fmaxf(s[1], s[3]);
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
-      x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
+      for (int nb = 0; nb < NB; ++nb) {
+        if (tok0 + g >= kv_len) s[nb][0] = s[nb][1] = -INFINITY;
+        if (tok0 + g + 8 >= kv_len) s[nb][2] = s[nb][3] = -INFINITY;
+      }
     }
-    const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
-    const float u0 = n0 == -INFINITY ? 0.f : n0;
-    const float u1 = n1 == -INFINITY ? 0.f : n1;
-    const float a0 = ex2(m0 - u0), a1 = ex2(m1 - u1);
-    const float p0 = ex2(s[0] - u0), p1 = ex2(s[1] - u1);
-    const float p2 = ex2(s[2] - u0), p3 = ex2(s[3] - u1);
-    d0 = d0 * a0 + p0 + p2;
-    d1 = d1 * a1 + p1 + p3;
-    m0 = n0;
-    m1 = n1;
+    if constexpr (kVerify) {
+      if (tok0 + kPageSize > draft0) {             // the page holds draft tokens
 #pragma unroll
-    for (int mt = 0; mt < 4; ++mt) {
-      o[mt][0] *= a0;
-      o[mt][1] *= a1;
-      o[mt][2] *= a0;
-      o[mt][3] *= a1;
+        for (int h8 = 0; h8 < 2; ++h8) {
+          const int u = tok0 + g + 8 * h8 - draft0;
+          if (u >= 0 && u < 64) {
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+              if (!((vis[nb][0] >> u) & 1)) s[nb][2 * h8] = -INFINITY;
+              if (!((vis[nb][1] >> u) & 1)) s[nb][2 * h8 + 1] = -INFINITY;
+            }
+          }
+        }
+      }
     }
-    const uint32_t pb0 = movmatrix_trans(pack_bf16(p0, p1));   // tokens 0..7
-    const uint32_t pb1 = movmatrix_trans(pack_bf16(p2, p3));   // tokens 8..15
+    uint32_t pb[NB][2];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+      float x0 = fmaxf(s[nb][0], s[nb][2]), x1 = fmaxf(s[nb][1], s[nb][3]);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
+        x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
+      }
+      const float n0 = fmaxf(m[nb][0], x0), n1 = fmaxf(m[nb][1], x1);
+      const float u0 = n0 == -INFINITY ? 0.f : n0;
+      const float u1 = n1 == -INFINITY ? 0.f : n1;
+      const float a0 = ex2(m[nb][0] - u0), a1 = ex2(m[nb][1] - u1);
+      const float p0 = ex2(s[nb][0] - u0), p1 = ex2(s[nb][1] - u1);
+      const float p2 = ex2(s[nb][2] - u0), p3 = ex2(s[nb][3] - u1);
+      d[nb][0] = d[nb][0] * a0 + p0 + p2;
+      d[nb][1] = d[nb][1] * a1 + p1 + p3;
+      m[nb][0] = n0;
+      m[nb][1] = n1;
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+        o[nb][mt][0] *= a0;
+        o[nb][mt][1] *= a1;
+        o[nb][mt][2] *= a0;
+        o[nb][mt][3] *= a1;
+      }
+      pb[nb][0] = movmatrix_trans(pack_bf16(p0, p1));   // tokens 0..7
+      pb[nb][1] = movmatrix_trans(pack_bf16(p2, p3));   // tokens 8..15
+    }
 
     uint32_t keep01 = 0xffffffffu, keep23 = 0xffffffffu;
     if (partial) {
@@ -267,47 +337,57 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       a[1] &= keep01;
       a[2] &= keep23;
       a[3] &= keep23;
-      mma_bf16_16816(o[mt], a, pb0, pb1);
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) mma_bf16_16816(o[nb][mt], a, pb[nb][0], pb[nb][1]);
     }
     __syncwarp();
     const int j = i + kStages;
     if (j < n_my) issue(j);
   }
 
-  // Full per-head sums.
+  // Full per-column sums.
 #pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    d0 += __shfl_xor_sync(0xffffffffu, d0, off);
-    d1 += __shfl_xor_sync(0xffffffffu, d1, off);
-  }
+  for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      d[nb][0] += __shfl_xor_sync(0xffffffffu, d[nb][0], off);
+      d[nb][1] += __shfl_xor_sync(0xffffffffu, d[nb][1], off);
+    }
   bad = bad || (__shfl_sync(0xffffffffu, lane_bad ? 1 : 0, 0) != 0);
 
   __syncthreads();   // every warp is done with its stages: alias them
-  MergeSmem &ms = *reinterpret_cast<MergeSmem *>(smem);
+  MergeSmem<NB> &ms = *reinterpret_cast<MergeSmem<NB> *>(smem);
   __shared__ int cta_bad;
   if (threadIdx.x == 0) cta_bad = 0;
-  if (g == 0) {
-    ms.m[warp][2 * t] = m0;
-    ms.m[warp][2 * t + 1] = m1;
-    ms.d[warp][2 * t] = d0;
-    ms.d[warp][2 * t + 1] = d1;
-  }
 #pragma unroll
-  for (int mt = 0; mt < 4; ++mt) {
-    ms.o[warp][2 * t][16 * mt + g] = o[mt][0];
-    ms.o[warp][2 * t + 1][16 * mt + g] = o[mt][1];
-    ms.o[warp][2 * t][16 * mt + 8 + g] = o[mt][2];
-    ms.o[warp][2 * t + 1][16 * mt + 8 + g] = o[mt][3];
+  for (int nb = 0; nb < NB; ++nb) {
+    const int c0 = nb * kHeadsPerTile + 2 * t;
+    if (g == 0) {
+      ms.m[warp][c0] = m[nb][0];
+      ms.m[warp][c0 + 1] = m[nb][1];
+      ms.d[warp][c0] = d[nb][0];
+      ms.d[warp][c0 + 1] = d[nb][1];
+    }
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+      ms.o[warp][c0][16 * mt + g] = o[nb][mt][0];
+      ms.o[warp][c0 + 1][16 * mt + g] = o[nb][mt][1];
+      ms.o[warp][c0][16 * mt + 8 + g] = o[nb][mt][2];
+      ms.o[warp][c0 + 1][16 * mt + 8 + g] = o[nb][mt][3];
+    }
   }
   __syncthreads();
   if (bad) atomicOr(&cta_bad, 1);
   __syncthreads();
   const bool failed = cta_bad != 0;
 
-  for (int item = threadIdx.x; item < kHeadsPerTile * (kHeadDim / 4); item += kNW * 32) {
+  const size_t stride = static_cast<size_t>(p.batch) * p.q_len * p.num_qo_heads;
+  for (int item = threadIdx.x; item < kCols * (kHeadDim / 4); item += kNW * 32) {
     const int hh = item / (kHeadDim / 4);
     const int dq = (item % (kHeadDim / 4)) * 4;
-    if (hh >= nheads) continue;
+    int head;
+    const long long ri = row_index<kVerify>(p, b, kvh, row0 + hh, head);
+    if (ri < 0) continue;
     float mx = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kNW; ++w) mx = fmaxf(mx, ms.m[w][hh]);
@@ -329,8 +409,7 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       acc[0] = acc[1] = acc[2] = acc[3] = NAN;
       lse2 = NAN;
     }
-    const int h = head0 + hh;
-    const size_t row = static_cast<size_t>(b) * p.num_qo_heads + h;
+    const size_t row = static_cast<size_t>(ri);
     if (nchunks <= 1) {
       uint2 packed;
       packed.x = pack_bf16(acc[0] * inv, acc[1] * inv);
@@ -338,7 +417,7 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       *reinterpret_cast<uint2 *>(p.out + row * kHeadDim + dq) = packed;
       if (dq == 0 && p.lse) p.lse[row] = lse2 * kLn2;
     } else {
-      const size_t wrow = static_cast<size_t>(chunk) * p.batch * p.num_qo_heads + row;
+      const size_t wrow = static_cast<size_t>(chunk) * stride + row;
       *reinterpret_cast<float4 *>(p.ws_o + wrow * kHeadDim + dq) =
           make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
       if (dq == 0) p.ws_lse[wrow] = lse2;
@@ -356,12 +435,13 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
   __syncthreads();
   if (!is_last) return;
   __threadfence();
-  const size_t stride = static_cast<size_t>(p.batch) * p.num_qo_heads;
-  for (int item = threadIdx.x; item < kHeadsPerTile * (kHeadDim / 4); item += kNW * 32) {
+  for (int item = threadIdx.x; item < kCols * (kHeadDim / 4); item += kNW * 32) {
     const int hh = item / (kHeadDim / 4);
     const int dq = (item % (kHeadDim / 4)) * 4;
-    if (hh >= nheads) continue;
-    const size_t row = static_cast<size_t>(b) * p.num_qo_heads + head0 + hh;
+    int head;
+    const long long ri = row_index<kVerify>(p, b, kvh, row0 + hh, head);
+    if (ri < 0) continue;
+    const size_t row = static_cast<size_t>(ri);
     float mx = -INFINITY, den = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
     bool poisoned = false;       // a chunk reported NaN (bad page or failed wait)
     for (int c = 0; c < nchunks; ++c) {
@@ -397,6 +477,21 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
   if (threadIdx.x == 0) p.counters[unit] = 0;
 }
 
+template <int NB, bool kVerify>
+cudaError_t launch_variant(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParams &p,
+                           cudaStream_t stream) {
+  cudaError_t err = cudaFuncSetAttribute(decode_kernel<NB, kVerify>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (err != cudaSuccess) return err;
+#if SA_DECODE_CHUNK_MAJOR
+  dim3 grid(p.num_kv_heads * p.head_blocks, p.batch, p.num_splits);
+#else
+  dim3 grid(p.num_splits, p.num_kv_heads * p.head_blocks, p.batch);
+#endif
+  decode_kernel<NB, kVerify><<<grid, kNW * 32, kSmemBytes, stream>>>(kmap, vmap, p);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 int decode_ctas_per_sm() {
@@ -409,16 +504,10 @@ int decode_max_splits() { return 1024; }
 cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParams &p,
                           cudaStream_t stream) {
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-  cudaError_t err = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemBytes);
-  if (err != cudaSuccess) return err;
-#if SA_DECODE_CHUNK_MAJOR
-  dim3 grid(p.num_kv_heads * p.head_blocks, p.batch, p.num_splits);
-#else
-  dim3 grid(p.num_splits, p.num_kv_heads * p.head_blocks, p.batch);
-#endif
-  decode_kernel<<<grid, kNW * 32, kSmemBytes, stream>>>(kmap, vmap, p);
-  return cudaGetLastError();
+  const bool verify = p.q_len > 1 || p.tree_mask != nullptr;
+  if (!verify && p.col_blocks == 1) return launch_variant<1, false>(kmap, vmap, p, stream);
+  if (p.col_blocks == 1) return launch_variant<1, true>(kmap, vmap, p, stream);
+  return launch_variant<2, true>(kmap, vmap, p, stream);
 }
 
 }  // namespace sa

@@ -15,28 +15,39 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 // ----------------------------------------------------------------- decode
+// Decode of q_len new tokens per request (q_len = 1: plain decode; q_len > 1:
+// speculative verification, bottom-right causal or a tree mask over the
+// request's last q_len keys).  The query rows of one KV head are ordered
+// (token, head in group): row r -> token r / group, head kvh*group + r % group.
 struct DecodeParams {
-  const uint16_t *q;            // bf16 [B][Hq][64]
+  const uint16_t *q;            // bf16 [B][q_len][Hq][64]
   const int32_t *page_table;    // [B][max_pages_per_seq]
   const int32_t *kv_lens;       // [B]
+  const uint64_t *tree_mask;    // [B][q_len] or null (causal)
   const float *sinks;           // [Hq]
-  uint16_t *out;                // bf16 [B][Hq][64]
-  float *lse;                   // [B][Hq] or null
+  uint16_t *out;                // bf16 [B][q_len][Hq][64]
+  float *lse;                   // [B][q_len][Hq] or null
   int *counters;                // [B][Hkv * head_blocks], zero between calls (splits > 1)
-  float *ws_o;                  // fp32 [splits][B][Hq][64] (splits > 1)
-  float *ws_lse;                // fp32 [splits][B][Hq]     (base-2 lse)
+  float *ws_o;                  // fp32 [splits][B][q_len][Hq][64] (splits > 1)
+  float *ws_lse;                // fp32 [splits][B][q_len][Hq]     (base-2 lse)
   float scale_log2;             // scale * log2(e)
   int max_pages_per_seq;
-  int batch, num_qo_heads, num_kv_heads, group, head_blocks;
+  int batch, q_len, num_qo_heads, num_kv_heads, group;
+  int rows;                     // q_len * group query rows per KV head
+  int col_blocks;               // 8-row column blocks per CTA (1 or 2)
+  int head_blocks;              // CTAs per (request, KV head, chunk) = ceil(rows / (8 col_blocks))
   int num_pages, num_splits, pages_per_chunk;
 };
+
+// Column blocks per CTA for q_len * group query rows per KV head.
+inline int decode_col_blocks(int rows) { return rows > 8 ? 2 : 1; }
 
 // Number of CTAs the decode kernel may keep resident per SM (for planning).
 int decode_ctas_per_sm();
 // Largest split count.
 int decode_max_splits();
 // Bytes at the start of the decode workspace that must be zero before a call.
-size_t decode_counter_bytes(int batch, int num_qo_heads, int num_kv_heads);
+size_t decode_counter_bytes(int batch, int num_qo_heads, int num_kv_heads, int q_len = 1);
 
 cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap,
                           const DecodeParams &p, cudaStream_t stream);

@@ -113,14 +113,23 @@ struct DecodePlan {
   size_t workspace_bytes = 0;
 };
 
+// CTA column blocks and head blocks of q_len tokens per request (q_len = 1:
+// plain decode, one 8-row column block per CTA).
+void decode_blocks(int q_len, int group, int *col_blocks, int *head_blocks) {
+  const int rows = q_len * group;
+  *col_blocks = q_len == 1 ? 1 : sa::decode_col_blocks(rows);
+  *head_blocks = ceil_div(rows, 8 * *col_blocks);
+}
+
 // Split count: by default enough (request, KV head, chunk) CTAs for a few
 // waves of the GPU, chunks of at least kMinPagesPerChunk pages; an explicit
 // count is honoured up to one page per chunk.
-DecodePlan plan_decode(int batch, int num_qo_heads, int num_kv_heads, int max_kv_len, int num_sms,
-                       int requested) {
+DecodePlan plan_decode(int batch, int q_len, int num_qo_heads, int num_kv_heads, int max_kv_len,
+                       int num_sms, int requested) {
   DecodePlan plan;
   const int group = num_qo_heads / num_kv_heads;
-  const int head_blocks = ceil_div(group, 8);
+  int col_blocks, head_blocks;
+  decode_blocks(q_len, group, &col_blocks, &head_blocks);
   const int max_pages = std::max(1, ceil_div(max_kv_len, kPageSize));
   int s;
   if (requested > 0) {
@@ -138,7 +147,7 @@ DecodePlan plan_decode(int batch, int num_qo_heads, int num_kv_heads, int max_kv
   if (plan.num_splits > 1) {
     const size_t units = static_cast<size_t>(batch) * num_kv_heads * head_blocks;
     plan.counters_bytes = (units * sizeof(int) + 255) & ~size_t(255);
-    const size_t rows = static_cast<size_t>(plan.num_splits) * batch * num_qo_heads;
+    const size_t rows = static_cast<size_t>(plan.num_splits) * batch * q_len * num_qo_heads;
     plan.workspace_bytes = plan.counters_bytes + rows * kHeadDim * sizeof(float) +
                            ((rows * sizeof(float) + 255) & ~size_t(255));
   }
@@ -148,9 +157,11 @@ DecodePlan plan_decode(int batch, int num_qo_heads, int num_kv_heads, int max_kv
 }  // namespace
 
 namespace sa {
-size_t decode_counter_bytes(int batch, int num_qo_heads, int num_kv_heads) {
-  if (batch <= 0 || num_kv_heads <= 0 || num_qo_heads <= 0) return 0;
-  const size_t units = static_cast<size_t>(batch) * num_kv_heads * ceil_div(num_qo_heads / num_kv_heads, 8);
+size_t decode_counter_bytes(int batch, int num_qo_heads, int num_kv_heads, int q_len) {
+  if (batch <= 0 || num_kv_heads <= 0 || num_qo_heads <= 0 || q_len <= 0) return 0;
+  int col_blocks, head_blocks;
+  decode_blocks(q_len, num_qo_heads / num_kv_heads, &col_blocks, &head_blocks);
+  const size_t units = static_cast<size_t>(batch) * num_kv_heads * head_blocks;
   return (units * sizeof(int) + 255) & ~size_t(255);
 }
 }  // namespace sa
@@ -183,38 +194,65 @@ int sinkattn_decode_plan(int batch, int num_qo_heads, int num_kv_heads, int head
     num_sms = device_sm_count();
     if (num_sms == 0) return fail_msg("no CUDA device to plan for");
   }
-  const DecodePlan plan = plan_decode(batch, num_qo_heads, num_kv_heads, max_kv_len, num_sms, *num_splits);
+  const DecodePlan plan = plan_decode(batch, 1, num_qo_heads, num_kv_heads, max_kv_len, num_sms, *num_splits);
   *num_splits = plan.num_splits;
   *workspace_bytes = plan.workspace_bytes;
   return SINKATTN_OK;
 }
 
-int sinkattn_decode(const void *q, const void *k_cache, const void *v_cache,
-                    const int32_t *page_table, int max_pages_per_seq, const int32_t *kv_lens,
-                    const float *sinks, float scale, void *out, float *lse, int batch,
-                    int num_qo_heads, int num_kv_heads, int head_dim, int page_size, int num_pages,
-                    int max_kv_len, int num_splits, void *workspace, size_t workspace_bytes,
-                    void *stream) {
+int sinkattn_verify_plan(int batch, int q_len, int num_qo_heads, int num_kv_heads, int head_dim,
+                         int page_size, int max_kv_len, int num_sms, int *num_splits,
+                         size_t *workspace_bytes) {
+  if (!num_splits || !workspace_bytes) return SINKATTN_INVALID_ARGUMENT;
   if (head_dim != kHeadDim || page_size != kPageSize) return SINKATTN_UNSUPPORTED;
-  if (batch < 0 || num_qo_heads <= 0 || num_kv_heads <= 0 || num_qo_heads % num_kv_heads ||
-      max_kv_len < 0 || num_splits < 0 || num_pages <= 0 || max_pages_per_seq <= 0 ||
-      !std::isfinite(scale))
+  if (batch < 0 || q_len < 1 || q_len > SINKATTN_MAX_VERIFY_TOKENS || num_qo_heads <= 0 ||
+      num_kv_heads <= 0 || max_kv_len < 0 || *num_splits < 0 || num_sms < 0 ||
+      num_qo_heads % num_kv_heads)
+    return SINKATTN_INVALID_ARGUMENT;
+  if (num_sms == 0) {
+    num_sms = device_sm_count();
+    if (num_sms == 0) return fail_msg("no CUDA device to plan for");
+  }
+  const DecodePlan plan = plan_decode(batch, q_len, num_qo_heads, num_kv_heads, max_kv_len, num_sms,
+                                      *num_splits);
+  *num_splits = plan.num_splits;
+  *workspace_bytes = plan.workspace_bytes;
+  return SINKATTN_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+// Decode of q_len tokens per request; q_len = 1 with no mask is plain decode.
+int decode_common(const void *q, const void *k_cache, const void *v_cache,
+                  const int32_t *page_table, int max_pages_per_seq, const int32_t *kv_lens,
+                  const uint64_t *tree_mask, const float *sinks, float scale, void *out, float *lse,
+                  int batch, int q_len, int num_qo_heads, int num_kv_heads, int head_dim,
+                  int page_size, int num_pages, int max_kv_len, int num_splits, void *workspace,
+                  size_t workspace_bytes, void *stream) {
+  if (head_dim != kHeadDim || page_size != kPageSize) return SINKATTN_UNSUPPORTED;
+  if (batch < 0 || q_len < 1 || q_len > SINKATTN_MAX_VERIFY_TOKENS || num_qo_heads <= 0 ||
+      num_kv_heads <= 0 || num_qo_heads % num_kv_heads || max_kv_len < 0 || num_splits < 0 ||
+      num_pages <= 0 || max_pages_per_seq <= 0 || !std::isfinite(scale))
     return SINKATTN_INVALID_ARGUMENT;
   if (batch == 0) return SINKATTN_OK;
   if (!q || !k_cache || !v_cache || !page_table || !kv_lens || !sinks || !out)
     return SINKATTN_INVALID_ARGUMENT;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
       !aligned(page_table, 4) || !aligned(kv_lens, 4) || !aligned(sinks, 4) ||
-      (lse && !aligned(lse, 4)))
+      (lse && !aligned(lse, 4)) || (tree_mask && !aligned(tree_mask, 8)))
     return SINKATTN_INVALID_ARGUMENT;
   const int group = num_qo_heads / num_kv_heads;
-  const int head_blocks = ceil_div(group, 8);
+  int col_blocks, head_blocks;
+  decode_blocks(q_len, group, &col_blocks, &head_blocks);
   if (batch > 65535 || static_cast<long long>(num_kv_heads) * head_blocks > 65535)
     return SINKATTN_UNSUPPORTED;
 
   const int sms = device_sm_count();
   if (sms == 0) return fail_msg("no CUDA device (SM count query failed)");
-  const DecodePlan plan = plan_decode(batch, num_qo_heads, num_kv_heads, max_kv_len, sms, num_splits);
+  const DecodePlan plan = plan_decode(batch, q_len, num_qo_heads, num_kv_heads, max_kv_len, sms,
+                                      num_splits);
   if (plan.num_splits > 1) {
     if (!workspace || workspace_bytes < plan.workspace_bytes) return SINKATTN_WORKSPACE_TOO_SMALL;
     if (!aligned(workspace, 256)) return SINKATTN_INVALID_ARGUMENT;
@@ -230,6 +268,7 @@ int sinkattn_decode(const void *q, const void *k_cache, const void *v_cache,
   p.q = static_cast<const uint16_t *>(q);
   p.page_table = page_table;
   p.kv_lens = kv_lens;
+  p.tree_mask = tree_mask;
   p.sinks = sinks;
   p.out = static_cast<uint16_t *>(out);
   p.lse = lse;
@@ -237,20 +276,50 @@ int sinkattn_decode(const void *q, const void *k_cache, const void *v_cache,
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     p.counters = reinterpret_cast<int *>(ws);
     p.ws_o = reinterpret_cast<float *>(ws + plan.counters_bytes);
-    p.ws_lse = p.ws_o + static_cast<size_t>(plan.num_splits) * batch * num_qo_heads * kHeadDim;
+    p.ws_lse = p.ws_o + static_cast<size_t>(plan.num_splits) * batch * q_len * num_qo_heads * kHeadDim;
   }
   p.scale_log2 = scale * sa::kLog2e;
   p.max_pages_per_seq = max_pages_per_seq;
   p.batch = batch;
+  p.q_len = q_len;
   p.num_qo_heads = num_qo_heads;
   p.num_kv_heads = num_kv_heads;
   p.group = group;
+  p.rows = q_len * group;
+  p.col_blocks = col_blocks;
   p.head_blocks = head_blocks;
   p.num_pages = num_pages;
   p.num_splits = plan.num_splits;
   p.pages_per_chunk = plan.pages_per_chunk;
   return cuda_status(sa::launch_decode(kmap, vmap, p, static_cast<cudaStream_t>(stream)),
                      "decode launch");
+}
+
+}  // namespace
+
+extern "C" {
+
+int sinkattn_decode(const void *q, const void *k_cache, const void *v_cache,
+                    const int32_t *page_table, int max_pages_per_seq, const int32_t *kv_lens,
+                    const float *sinks, float scale, void *out, float *lse, int batch,
+                    int num_qo_heads, int num_kv_heads, int head_dim, int page_size, int num_pages,
+                    int max_kv_len, int num_splits, void *workspace, size_t workspace_bytes,
+                    void *stream) {
+  return decode_common(q, k_cache, v_cache, page_table, max_pages_per_seq, kv_lens, nullptr, sinks,
+                       scale, out, lse, batch, 1, num_qo_heads, num_kv_heads, head_dim, page_size,
+                       num_pages, max_kv_len, num_splits, workspace, workspace_bytes, stream);
+}
+
+int sinkattn_verify(const void *q, const void *k_cache, const void *v_cache,
+                    const int32_t *page_table, int max_pages_per_seq, const int32_t *kv_lens,
+                    const uint64_t *tree_mask, const float *sinks, float scale, void *out,
+                    float *lse, int batch, int q_len, int num_qo_heads, int num_kv_heads,
+                    int head_dim, int page_size, int num_pages, int max_kv_len, int num_splits,
+                    void *workspace, size_t workspace_bytes, void *stream) {
+  return decode_common(q, k_cache, v_cache, page_table, max_pages_per_seq, kv_lens, tree_mask,
+                       sinks, scale, out, lse, batch, q_len, num_qo_heads, num_kv_heads, head_dim,
+                       page_size, num_pages, max_kv_len, num_splits, workspace, workspace_bytes,
+                       stream);
 }
 
 int sinkattn_prefill(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,

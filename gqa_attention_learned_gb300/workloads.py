@@ -201,3 +201,37 @@ def mixed_batch(seed=4, num_decode=32, num_extend=4, extend_len=2048,
         extend=dict(q=q_ext, cu_seqlens_q=cu, page_table=table[num_decode:].contiguous(),
                     kv_lens=kv[num_decode:].contiguous(), max_q_len=extend_len,
                     max_kv_len=int(ext_lens.max())))
+
+
+def random_tree_masks(rng, batch, q_len):
+    """Draft trees for verification: node u > 0 hangs off a uniformly drawn
+    earlier node or directly off the accepted prefix; node 0 hangs off the
+    prefix.  Row i of a request holds the bits of i and of its ancestors
+    (int64 [batch, q_len], bit patterns of uint64)."""
+    masks = np.zeros((batch, q_len), dtype=np.uint64)
+    for b in range(batch):
+        parent = [-1] + [int(rng.integers(-1, u)) for u in range(1, q_len)]
+        for u in range(q_len):
+            bits, a = 0, u
+            while a >= 0:
+                bits |= 1 << a
+                a = parent[a]
+            masks[b, u] = bits
+    return torch.from_numpy(masks.view(np.int64))
+
+
+def verify_batch(seed=5, batch=64, q_len=4, num_qo_heads=64, num_kv_heads=8, min_len=1,
+                 max_len=4096, tree=False, special_sinks=True):
+    """Verification of q_len draft tokens per request (speculative decoding):
+    the drafts are the last q_len keys of each request's paged KV, whose
+    length is ~ U{max(min_len, q_len)..max_len}; with `tree`, each request
+    carries a random draft tree's masks, else verification is causal."""
+    rng = np.random.default_rng(seed)
+    kv_lens = rng.integers(max(min_len, q_len), max_len + 1, size=batch)
+    q = _bf16(_normal(rng, (batch, q_len, num_qo_heads, HEAD_DIM)))
+    sinks = gpt_oss_sinks(rng, num_qo_heads, 2.0, special_sinks)
+    masks = random_tree_masks(rng, batch, q_len) if tree else None
+    pool = paged_pool(rng, kv_lens, num_kv_heads)
+    return dict(name="verify", num_qo_heads=num_qo_heads, num_kv_heads=num_kv_heads,
+                head_dim=HEAD_DIM, scale=0.125, q=q, q_len=q_len, sinks=sinks, tree_mask=masks,
+                max_kv_len=int(max(kv_lens)), **pool)

@@ -125,6 +125,44 @@ SINKATTN_API int sinkattn_decode(const void *q, const void *k_cache, const void 
                     void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Verification of draft tokens ("Accelerating Sonar through speculation",
+ * Perplexity blog: sections "Target-Draft" and "MTP" run the target model
+ * over the q_len = k + 1 newest tokens of every request in one pass --
+ * single-token MTP verifies 2 per request -- and section "EAGLE" verifies a
+ * tree of drafts, which needs a custom attention mask).  Every request has
+ * exactly q_len new tokens, already written as the LAST q_len keys of its
+ * paged KV.  Query token i (0-based) of request b sees
+ *   - every key j < kv_len - q_len (the accepted prefix), and
+ *   - draft key kv_len - q_len + u for u in [0, q_len) when
+ *       tree_mask == NULL : u <= i                 (causal, aligned at the end)
+ *       tree_mask != NULL : bit u of tree_mask[b][i] is set
+ *     (a token sees itself only if its own bit is set).
+ * The mask covers the draft tokens only, so the prefix costs no mask work.
+ *   q          : bf16 [batch][q_len][num_qo_heads][head_dim]
+ *   tree_mask  : uint64 [batch][q_len], 8-byte aligned, or NULL
+ *   out        : bf16 [batch][q_len][num_qo_heads][head_dim]
+ *   lse        : fp32 [batch][q_len][num_qo_heads]; may be NULL
+ *   q_len      : 1 .. SINKATTN_MAX_VERIFY_TOKENS
+ *   other arguments, the split plan (sinkattn_verify_plan) and the workspace
+ *   rules: as for sinkattn_decode.  kv_len < q_len makes the request's rows
+ *   NaN.  q_len = 1 with tree_mask = NULL computes what sinkattn_decode does.
+ */
+#define SINKATTN_MAX_VERIFY_TOKENS 64
+
+SINKATTN_API int sinkattn_verify_plan(int batch, int q_len, int num_qo_heads, int num_kv_heads,
+                         int head_dim, int page_size, int max_kv_len, int num_sms,
+                         int *num_splits, size_t *workspace_bytes);
+
+SINKATTN_API int sinkattn_verify(const void *q, const void *k_cache, const void *v_cache,
+                    const int32_t *page_table, int max_pages_per_seq,
+                    const int32_t *kv_lens, const uint64_t *tree_mask,
+                    const float *sinks, float scale, void *out, float *lse,
+                    int batch, int q_len, int num_qo_heads, int num_kv_heads,
+                    int head_dim, int page_size, int num_pages, int max_kv_len,
+                    int num_splits, void *workspace, size_t workspace_bytes,
+                    void *stream);
+
+/*
  * Causal prefill over ragged sequences packed along the token axis.
  *   q          : bf16 [total_tokens][num_qo_heads][head_dim]
  *   k, v       : bf16 [total_tokens][num_kv_heads][head_dim]

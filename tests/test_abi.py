@@ -116,3 +116,41 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(sa, "_lib", None)
     with pytest.raises(RuntimeError):
         sa.load()
+
+
+def test_verify_plan(lib):
+    # q_len = 1 plans exactly like decode
+    assert sa.verify_plan(64, 1, 64, 8, 4096, num_sms=152) == sa.decode_plan(64, 64, 8, 4096,
+                                                                             num_sms=152)
+    # 4 tokens x 8 heads = 32 rows per KV head = 2 CTAs of 16 rows; the
+    # workspace holds one counter per (request, KV head, CTA) and one
+    # (o, lse) slot per chunk and query row
+    s, ws = sa.verify_plan(8, 4, 64, 8, 131072, num_splits=8, num_sms=152)
+    counters = 8 * 8 * 2 * 4               # batch x Hkv x CTAs per KV head, int32
+    rows = 8 * 8 * 4 * 64                  # chunks x batch x q_len x Hq
+    assert s == 8
+    assert ws == counters + rows * 64 * 4 + rows * 4
+    with pytest.raises(sa.SinkAttnError) as e:
+        sa.verify_plan(1, sa.MAX_VERIFY_TOKENS + 1, 64, 8, 4096, num_sms=152)
+    assert e.value.status == sa.INVALID_ARGUMENT
+    with pytest.raises(sa.SinkAttnError) as e:
+        sa.verify_plan(1, 0, 64, 8, 4096, num_sms=152)
+    assert e.value.status == sa.INVALID_ARGUMENT
+
+
+def test_verify_rejects_on_host(lib):
+    fake = ctypes.c_void_p(0x1000)
+
+    def call(**kw):
+        a = dict(q=fake, k=fake, v=fake, table=fake, maxp=1, lens=fake, mask=None, sinks=fake,
+                 scale=0.125, out=fake, lse=None, batch=1, q_len=2, hq=8, hkv=1, d=64, page=16,
+                 pages=1, maxkv=16, splits=1, ws=None, wsb=0, stream=None)
+        a.update(kw)
+        return lib.sinkattn_verify(*a.values())
+
+    assert call(d=128) == sa.UNSUPPORTED
+    assert call(q_len=0) == sa.INVALID_ARGUMENT
+    assert call(q_len=sa.MAX_VERIFY_TOKENS + 1) == sa.INVALID_ARGUMENT
+    assert call(mask=ctypes.c_void_p(0x1004)) == sa.INVALID_ARGUMENT     # misaligned mask
+    assert call(q=None) == sa.INVALID_ARGUMENT
+    assert call(batch=0) == sa.OK

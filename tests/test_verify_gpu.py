@@ -1,0 +1,118 @@
+"""GPU parity of sinkattn_verify (draft-token verification) against the
+float64 oracle, through the C ABI.
+
+"Accelerating Sonar through speculation" (Perplexity blog): sections
+"Target-Draft" and "MTP" verify the k + 1 newest tokens of every request in
+one pass; section "EAGLE" verifies a draft tree with a custom mask.
+
+Cases: causal verification with 1..16 tokens for GQA groups 1..16, against
+the oracle and (for one token) bitwise against sinkattn_decode; random draft
+trees of 3..64 nodes; forced chunking (splits 1, 3, 1000); the gpt-oss-20b
+batch with 4 tokens per request (sampled requests); rows that see no key;
+requests with fewer keys than new tokens.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import gqa_attention_learned_gb300 as sa
+import oracle
+from gqa_attention_learned_gb300 import workloads
+from tolerances import Bf16Pool, assert_lse_close, assert_out_close, to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def run_verify(w, **kw):
+    q, kc, vc, table, lens, sinks = [w[n].to(DEV) for n in
+                                     ("q", "k_cache", "v_cache", "page_table", "kv_lens", "sinks")]
+    mask = w.get("tree_mask")
+    out, lse = sa.verify(q, kc, vc, table, lens, sinks, w["scale"], w["max_kv_len"],
+                         tree_mask=None if mask is None else mask.to(DEV), **kw)
+    torch.cuda.synchronize()
+    return out.cpu(), lse.cpu()
+
+
+def ref_verify(w, requests=None):
+    reqs = slice(None) if requests is None else list(requests)
+    mask = w.get("tree_mask")
+    return oracle.verify(to_np(w["q"][reqs]), Bf16Pool(w["k_cache"]), Bf16Pool(w["v_cache"]),
+                         w["page_table"].numpy()[reqs], w["kv_lens"].numpy()[reqs],
+                         w["sinks"].numpy().astype(np.float64), w["scale"],
+                         tree_mask=None if mask is None else mask.numpy()[reqs])
+
+
+@pytest.mark.parametrize("q_len", [1, 2, 3, 4, 7, 16])
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (4, 1), (16, 1)])
+def test_causal_verify_small(q_len, hq, hkv):
+    w = workloads.verify_batch(seed=100 + q_len, batch=6, q_len=q_len, num_qo_heads=hq,
+                               num_kv_heads=hkv, max_len=300)
+    out, lse = run_verify(w)
+    ro, rl = ref_verify(w)
+    assert_out_close(out, ro)
+    assert_lse_close(lse, rl)
+
+
+@pytest.mark.parametrize("q_len", [3, 8, 16, 64])
+def test_tree_verify(q_len):
+    w = workloads.verify_batch(seed=200 + q_len, batch=5, q_len=q_len, num_qo_heads=16,
+                               num_kv_heads=2, max_len=400, tree=True)
+    out, lse = run_verify(w)
+    ro, rl = ref_verify(w)
+    assert_out_close(out, ro)
+    assert_lse_close(lse, rl)
+
+
+@pytest.mark.parametrize("splits", [1, 3, 1000])
+def test_verify_split_counts(splits):
+    w = workloads.verify_batch(seed=7, batch=4, q_len=5, num_qo_heads=8, num_kv_heads=1,
+                               min_len=100, max_len=2000, tree=True)
+    out, lse = run_verify(w, num_splits=splits)
+    ro, rl = ref_verify(w)
+    assert_out_close(out, ro)
+    assert_lse_close(lse, rl)
+
+
+def test_one_token_is_bitwise_decode():
+    w = workloads.verify_batch(seed=9, batch=16, q_len=1, max_len=3000)
+    d = dict(w, q=w["q"][:, 0].contiguous())
+    args = [d[n].to(DEV) for n in ("q", "k_cache", "v_cache", "page_table", "kv_lens", "sinks")]
+    do, dl = sa.decode(*args, d["scale"], d["max_kv_len"])
+    vo, vl = run_verify(w)
+    mo, ml = run_verify(dict(w, tree_mask=torch.ones(16, 1, dtype=torch.int64)))
+    torch.cuda.synchronize()
+    for o, l in ((vo, vl), (mo, ml)):
+        assert torch.equal(o[:, 0], do.cpu())
+        assert torch.equal(l[:, 0], dl.cpu())
+
+
+def test_gpt_oss_20b_batch_four_tokens_sampled():
+    w = workloads.verify_batch(q_len=4)
+    out, lse = run_verify(w)
+    reqs = [0, 1, 17, 33, 62, 63]
+    ro, rl = ref_verify(w, reqs)
+    assert_out_close(out[reqs], ro)
+    assert_lse_close(lse[reqs], rl)
+    assert torch.isfinite(out.float()).all() and not torch.isnan(lse).any()
+
+
+def test_rows_that_see_no_key_and_short_requests():
+    w = workloads.verify_batch(seed=11, batch=4, q_len=3, num_qo_heads=8, num_kv_heads=2,
+                               max_len=50, tree=True)
+    lens = w["kv_lens"].clone()
+    lens[0] = 3                       # no prefix: the drafts are the whole request
+    lens[2] = 2                       # fewer keys than new tokens: NaN rows
+    mask = w["tree_mask"].clone()
+    mask[0, 1] = 0                    # sees nothing: out = 0, lse = sink
+    w = dict(w, kv_lens=lens, tree_mask=mask)
+    out, lse = run_verify(w)
+    assert torch.isnan(out[2].float()).all() and torch.isnan(lse[2]).all()
+    ok = [0, 1, 3]
+    ro, rl = ref_verify(w, ok)
+    assert_out_close(out[ok], ro)
+    assert_lse_close(lse[ok], rl)
+    assert torch.equal(out[0, 1].float(), torch.zeros(8, 64))
+    sinks = w["sinks"]
+    assert torch.equal(torch.isinf(lse[0, 1]), torch.isinf(sinks))
