@@ -303,20 +303,26 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       const float n0 = fmaxf(m[nb][0], x0), n1 = fmaxf(m[nb][1], x1);
       const float u0 = n0 == -INFINITY ? 0.f : n0;
       const float u1 = n1 == -INFINITY ? 0.f : n1;
-      const float a0 = ex2(m[nb][0] - u0), a1 = ex2(m[nb][1] - u1);
       const float p0 = ex2(s[nb][0] - u0), p1 = ex2(s[nb][1] - u1);
       const float p2 = ex2(s[nb][2] - u0), p3 = ex2(s[nb][3] - u1);
-      d[nb][0] = d[nb][0] * a0 + p0 + p2;
-      d[nb][1] = d[nb][1] * a1 + p1 + p3;
+      // o and d only need rescaling when a running max grew; otherwise the
+      // factor is exactly 1 and the warp skips the multiplies
+      if (__any_sync(0xffffffffu, n0 > m[nb][0] || n1 > m[nb][1])) {
+        const float a0 = ex2(m[nb][0] - u0), a1 = ex2(m[nb][1] - u1);
+        d[nb][0] *= a0;
+        d[nb][1] *= a1;
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+          o[nb][mt][0] *= a0;
+          o[nb][mt][1] *= a1;
+          o[nb][mt][2] *= a0;
+          o[nb][mt][3] *= a1;
+        }
+      }
+      d[nb][0] += p0 + p2;
+      d[nb][1] += p1 + p3;
       m[nb][0] = n0;
       m[nb][1] = n1;
-#pragma unroll
-      for (int mt = 0; mt < 4; ++mt) {
-        o[nb][mt][0] *= a0;
-        o[nb][mt][1] *= a1;
-        o[nb][mt][2] *= a0;
-        o[nb][mt][3] *= a1;
-      }
       pb[nb][0] = movmatrix_trans(pack_bf16(p0, p1));   // tokens 0..7
       pb[nb][1] = movmatrix_trans(pack_bf16(p2, p3));   // tokens 8..15
     }

@@ -21,6 +21,7 @@ using sa::kPageSize;
 constexpr int kMaxDevices = 64;
 constexpr int kMinPagesPerChunk = 16;   // keeps merge traffic under ~3% of KV
 constexpr int kWavesTarget = 4;
+constexpr int kVerifyWavesTarget = 2;
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -137,8 +138,15 @@ DecodePlan plan_decode(int batch, int q_len, int num_qo_heads, int num_kv_heads,
   } else {
     const long long units = static_cast<long long>(batch) * num_kv_heads * head_blocks;
     const long long slots = static_cast<long long>(std::max(num_sms, 1)) * sa::decode_ctas_per_sm();
-    s = static_cast<int>(std::min<long long>((kWavesTarget * slots + units - 1) / std::max(units, 1ll),
-                                             1 << 20));
+    if (col_blocks == 1) {
+      s = static_cast<int>(std::min<long long>((kWavesTarget * slots + units - 1) / std::max(units, 1ll),
+                                               1 << 20));
+    } else {
+      // a CTA with two column blocks does twice the work per page, which
+      // makes the kernel throughput-bound: fewer, longer chunks (measured)
+      s = static_cast<int>(std::min<long long>(kVerifyWavesTarget * slots / std::max(units, 1ll),
+                                               1 << 20));
+    }
     s = std::min(s, std::max(1, max_pages / kMinPagesPerChunk));
   }
   s = std::max(1, std::min({s, sa::decode_max_splits(), max_pages}));
