@@ -287,6 +287,63 @@ def run_decode_arm(args, rank, dev):
                                 steps=kv_steps))
 
 
+def run_graph_decode(args, rank, dev, peaks):
+    """The headline decode step replayed from CUDA graphs (one per KV pool
+    copy) instead of launched from Python: same kernel, no host work."""
+    import torch
+
+    import gqa_attention_learned_gb300 as sa
+    from gqa_attention_learned_gb300 import workloads
+
+    w = workloads.decode_batch(seed=1 + 1000 * rank)
+    hq, hkv = w["num_qo_heads"], w["num_kv_heads"]
+    lens = [int(x) for x in w["kv_lens"]]
+    nbytes = decode_bytes(lens, hq, hkv)
+    q = w["q"].to(dev)
+    pools = [(w["k_cache"].to(dev), w["v_cache"].to(dev))]
+    pools.append((pools[0][0].clone(), pools[0][1].clone()))
+    table, kv_lens, sinks = w["page_table"].to(dev), w["kv_lens"].to(dev), w["sinks"].to(dev)
+    max_kv = w["max_kv_len"]
+    _, ws_bytes = sa.decode_plan(64, hq, hkv, max_kv)
+    ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[0], hq, dtype=torch.float32, device=dev)
+
+    def call(i):
+        kc, vc = pools[i & 1]
+        sa.decode(q, kc, vc, table, kv_lens, sinks, w["scale"], max_kv, out=out, lse=lse,
+                  workspace=ws)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call(0)
+        call(1)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graphs = []
+    for i in range(2):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            call(i)
+        graphs.append(g)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        graphs[i & 1].replay()
+
+    steps = max(100, args.steps // 2)
+    secs = _time_steps(torch, step, steps, args.warmup, stream)
+    _, t, bps = aggregate(nbytes * steps, secs, dev)
+    del graphs, pools
+    torch.cuda.empty_cache()
+    return dict(workload=DECODE_WORKLOAD + " (CUDA graph replay)", steps=steps,
+                ms_per_step=1e3 * t / steps, value=round(bps / 1e9, 2), unit="GB/s",
+                frac_of_hbm=round(bps / 1e9 / peaks["hbm_gbs"], 4),
+                note="plan from host-side sizes; chunks per request derived on the device from "
+                     "kv_lens, so the captured launch serves new lengths and page tables")
+
+
 def run_long_decode(args, rank, dev):
     import torch
 
@@ -482,6 +539,8 @@ def gpu_arm(args):
     if not args.quick:
         if "long" in sections:
             extra["long_decode"] = run_long_decode(args, rank, dev)
+        if "graph" in sections:
+            extra["graph_decode"] = run_graph_decode(args, rank, dev, peaks)
         if "verify" in sections:
             extra["verify"] = run_verify(args, rank, dev, peaks)
         if "prefill" in sections:
@@ -631,7 +690,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--splits", type=int, default=0, help="decode split count (0 = planned)")
     ap.add_argument("--quick", action="store_true", help="headline decode only")
-    ap.add_argument("--sections", default="long,verify,prefill,mixed",
+    ap.add_argument("--sections", default="graph,long,verify,prefill,mixed",
                     help="extra sections after the headline decode")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
