@@ -77,6 +77,14 @@ def verify_bytes(kv_lens, q_len, num_qo_heads, num_kv_heads, tree, head_dim=HEAD
             + b * 4 + pages * 4 + (b * q_len * 8 if tree else 0))
 
 
+def prologue_bytes(tokens, num_qo_heads, num_kv_heads, head_dim=HEAD_DIM):
+    """Algorithmic bytes of the prologue: the qkv rows and the token's position
+    and slot read once, q written once, k and v written to their cache slot,
+    plus the bias row."""
+    heads = num_qo_heads + 2 * num_kv_heads
+    return tokens * (2 * heads * head_dim * 2 + 8) + heads * head_dim * 2
+
+
 def prefill_flops(seqlens, num_qo_heads, head_dim=HEAD_DIM):
     """QK^T and PV over the causal (lower-triangular incl. diagonal) pairs."""
     return sum(4 * head_dim * num_qo_heads * n * (n + 1) // 2 for n in seqlens)
@@ -422,6 +430,68 @@ def run_verify(args, rank, dev, peaks):
                 kernel="decode_kernel<2, true> (rows = tokens x heads of a KV head)", runs=res)
 
 
+def run_prologue(args, rank, dev, peaks):
+    import numpy as np
+    import torch
+
+    import gqa_attention_learned_gb300 as sa
+    from gqa_attention_learned_gb300 import workloads
+
+    inv, ms = sa.yarn_table()                     # base 150000, factor 32, L 4096, beta 32 / 1
+    pre = workloads.ragged_prefill(seed=3 + 1000 * rank)
+    cu = [int(x) for x in pre["cu_seqlens"]]
+    lens = [b - a for a, b in zip(cu, cu[1:])]
+    res = {}
+    for label, seq_lens, starts in (("prefill 4 sequences", lens, [0] * len(lens)),
+                                    ("decode 64 tokens", [1] * 64,
+                                     [int(x) for x in np.random.default_rng(1).integers(0, 4096, 64)])):
+        w = workloads.prologue_batch(seq_lens, starts, seed=6 + 1000 * rank)
+        tokens = sum(seq_lens)
+        nbytes = prologue_bytes(tokens, 64, 8)
+        qkv, bias = w["qkv"].to(dev), w["bias"].to(dev)
+        pos, slots = w["positions"].to(dev), w["slot_mapping"].to(dev)
+        kc, vc = w["k_cache"].to(dev), w["v_cache"].to(dev)
+        q_out = torch.empty(tokens, 64, 64, dtype=torch.bfloat16, device=dev)
+        stream = torch.cuda.current_stream()
+
+        def call(qkv=qkv, bias=bias, pos=pos, slots=slots, kc=kc, vc=vc, q_out=q_out):
+            sa.qkv_prologue(qkv, bias, pos, slots, inv, ms, kc, vc, 64, 8, q_out=q_out)
+
+        # launches replayed from a CUDA graph (10 per replay), so the small
+        # case measures the device, not the Python call
+        per_graph = 10
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            call()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(per_graph):
+                call()
+
+        def step(i, g=g):
+            g.replay()
+
+        steps = max(10, args.steps // 200)
+        secs = _time_steps(torch, step, steps, args.warmup, stream)
+        _, t, bps = aggregate(nbytes * steps * per_graph, secs, dev)
+        t /= per_graph
+        res[label] = dict(tokens=tokens, bytes_per_step=nbytes, ms_per_step=1e3 * t / steps,
+                          value=round(bps / 1e9, 2), unit="GB/s",
+                          frac_of_hbm=round(bps / 1e9 / peaks["hbm_gbs"], 4))
+        del qkv, kc, vc, q_out, g
+        torch.cuda.empty_cache()
+    return dict(workload="attention prologue (QKV bias + YaRN rotary on q/k + paged k/v write), "
+                         "64 q / 8 KV heads, head_dim 64, bf16; YaRN base 150000, factor 32, "
+                         "original context 4096, beta 32 / 1 (the pages give no values)",
+                kernel="prologue_kernel",
+                note="timed as CUDA-graph replays of 10 launches; the decode-sized batch "
+                     "(1.3 MB) is L2-resident",
+                runs=res)
+
+
 def run_prefill(args, rank, dev, peaks):
     import torch
 
@@ -543,6 +613,8 @@ def gpu_arm(args):
             extra["graph_decode"] = run_graph_decode(args, rank, dev, peaks)
         if "verify" in sections:
             extra["verify"] = run_verify(args, rank, dev, peaks)
+        if "prologue" in sections:
+            extra["prologue"] = run_prologue(args, rank, dev, peaks)
         if "prefill" in sections:
             extra["prefill"] = run_prefill(args, rank, dev, peaks)
         if "mixed" in sections:
@@ -690,7 +762,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--splits", type=int, default=0, help="decode split count (0 = planned)")
     ap.add_argument("--quick", action="store_true", help="headline decode only")
-    ap.add_argument("--sections", default="graph,long,verify,prefill,mixed",
+    ap.add_argument("--sections", default="graph,long,verify,prologue,prefill,mixed",
                     help="extra sections after the headline decode")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

@@ -38,12 +38,19 @@ SIGNATURES = {
     "sinkattn_prefill_paged": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _vp, _c_int,
                                         _vp, _c_int, _c_int, _vp, _c_float, _vp, _vp, _c_int,
                                         _c_int, _c_int, _c_int, _vp]),
+    "sinkattn_yarn_table": (_c_int, [_c_int, ctypes.c_double, ctypes.c_double, ctypes.c_double,
+                                     ctypes.c_double, ctypes.c_double,
+                                     ctypes.POINTER(_c_float), ctypes.POINTER(_c_float)]),
+    "sinkattn_qkv_prologue": (_c_int, [_vp, _vp, _vp, _vp, ctypes.POINTER(_c_float), _c_float,
+                                       _c_int, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
+                                       _c_int, _c_int, _vp]),
     "sinkattn_decode_static_scratch": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _vp, _c_float,
                                                 _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
                                                 _c_int, _c_int, _c_int, _vp]),
 }
 
 STATIC_SCRATCH_BYTES = 16 << 20
+ROPE_HALF, ROPE_INTERLEAVED = 0, 1
 MAX_VERIFY_TOKENS = 64
 
 _lib = None
@@ -282,3 +289,45 @@ def decode_static_scratch(q, k_cache, v_cache, page_table, kv_lens, sinks, scale
             _ptr(kv_lens), _ptr(sinks), float(scale), _ptr(out), _ptr(lse), batch, hq, hkv, d,
             page, num_pages, int(max_kv_len), int(num_splits), _stream(stream)))
     return out, lse
+
+
+def yarn_table(head_dim=64, base=150000.0, factor=32.0, original_context=4096, beta_fast=32.0,
+               beta_slow=1.0):
+    """(inv_freq list of head_dim/2 floats, mscale): YaRN-scaled rotary
+    frequencies and magnitude factor (host only)."""
+    freq = (_c_float * (head_dim // 2))()
+    ms = _c_float(0)
+    _check("sinkattn_yarn_table",
+           load().sinkattn_yarn_table(head_dim, float(base), float(factor), float(original_context),
+                                      float(beta_fast), float(beta_slow), freq, ctypes.byref(ms)))
+    return list(freq), ms.value
+
+
+def qkv_prologue(qkv, bias, positions, slot_mapping, inv_freq, mscale, k_cache, v_cache,
+                 num_qo_heads, num_kv_heads, *, rope_style=ROPE_HALF, q_out=None, stream=None):
+    """QKV bias + rotary encoding of q and k + k/v written into the paged
+    cache, one launch.  qkv [T, (Hq + 2 Hkv) * 64] bf16; bias same width or
+    None; positions, slot_mapping [T] int32 (slot = page * 16 + offset, < 0:
+    no write); inv_freq: sequence of 32 floats (host).  Returns q_out
+    [T, Hq, 64] bf16; k_cache / v_cache are written in place."""
+    dev = qkv.device
+    _want(qkv, "qkv", torch.bfloat16, 2)
+    if bias is not None:
+        _want(bias, "bias", torch.bfloat16, 1, dev)
+    _want(positions, "positions", torch.int32, 1, dev)
+    _want(slot_mapping, "slot_mapping", torch.int32, 1, dev)
+    _want(k_cache, "k_cache", torch.bfloat16, 4, dev)
+    _want(v_cache, "v_cache", torch.bfloat16, 4, dev)
+    tokens = qkv.shape[0]
+    num_pages, hkv, page, d = k_cache.shape
+    if hkv != num_kv_heads or qkv.shape[1] != (num_qo_heads + 2 * num_kv_heads) * d:
+        raise ValueError("qkv width / cache heads disagree with the head counts")
+    freq = (_c_float * (d // 2))(*[float(x) for x in inv_freq])
+    if q_out is None:
+        q_out = torch.empty(tokens, num_qo_heads, d, dtype=torch.bfloat16, device=dev)
+    with torch.cuda.device(dev):
+        _check("sinkattn_qkv_prologue", load().sinkattn_qkv_prologue(
+            _ptr(qkv), _ptr(bias), _ptr(positions), _ptr(slot_mapping), freq, float(mscale),
+            int(rope_style), _ptr(q_out), _ptr(k_cache), _ptr(v_cache), tokens, num_qo_heads,
+            num_kv_heads, d, page, num_pages, _stream(stream)))
+    return q_out

@@ -74,4 +74,20 @@ cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap,
                            const CUtensorMap &vmap, const PrefillParams &p,
                            cudaStream_t stream);
 
+// --------------------------------------------------------------- prologue
+struct PrologueParams {
+  const uint16_t *qkv;           // bf16 [T][(Hq + 2 Hkv) * 64], q heads, then k, then v
+  const uint16_t *bias;          // bf16 [(Hq + 2 Hkv) * 64] or null
+  const int32_t *positions;      // [T]
+  const int32_t *slot_mapping;   // [T]: page * 16 + slot; < 0 or past the pool: no write
+  uint16_t *q_out;               // bf16 [T][Hq][64]
+  uint16_t *k_cache, *v_cache;   // bf16 [num_pages][Hkv][16][64]
+  float inv_freq[kHeadDim / 2];  // rotary angular frequencies
+  float mscale;                  // magnitude factor on cos and sin
+  int num_tokens, num_qo_heads, num_kv_heads, num_pages;
+  int interleaved;               // 0: pairs (i, i + 32); 1: pairs (2i, 2i + 1)
+};
+
+cudaError_t launch_prologue(const PrologueParams &p, cudaStream_t stream);
+
 }  // namespace sa

@@ -419,4 +419,62 @@ int sinkattn_prefill_paged(const void *q, const int32_t *cu_seqlens_q, int num_s
                      "prefill launch");
 }
 
+int sinkattn_yarn_table(int head_dim, double base, double factor, double original_context,
+                        double beta_fast, double beta_slow, float *inv_freq, float *mscale) {
+  if (!inv_freq || !mscale || head_dim <= 0 || head_dim % 2 || !(base > 1.0) ||
+      !(factor >= 1.0) || !(original_context > 0.0) || !(beta_fast > beta_slow) ||
+      !std::isfinite(base) || !std::isfinite(factor) || !std::isfinite(original_context))
+    return SINKATTN_INVALID_ARGUMENT;
+  const double two_pi = 6.283185307179586476925286766559;
+  for (int d = 0; d < head_dim / 2; ++d) {
+    const double theta = std::pow(base, -2.0 * d / head_dim);
+    const double turns = original_context * theta / two_pi;   // rotations over the original context
+    double ramp = (turns - beta_slow) / (beta_fast - beta_slow);
+    ramp = std::min(1.0, std::max(0.0, ramp));
+    inv_freq[d] = static_cast<float>(theta * ramp + theta / factor * (1.0 - ramp));
+  }
+  *mscale = static_cast<float>(0.1 * std::log(factor) + 1.0);
+  return SINKATTN_OK;
+}
+
+int sinkattn_qkv_prologue(const void *qkv, const void *bias, const int32_t *positions,
+                          const int32_t *slot_mapping, const float *inv_freq, float mscale,
+                          int rope_style, void *q_out, void *k_cache, void *v_cache,
+                          int num_tokens, int num_qo_heads, int num_kv_heads, int head_dim,
+                          int page_size, int num_pages, void *stream) {
+  if (head_dim != kHeadDim || page_size != kPageSize) return SINKATTN_UNSUPPORTED;
+  if (num_tokens < 0 || num_qo_heads <= 0 || num_kv_heads <= 0 || num_pages <= 0 ||
+      (rope_style != SINKATTN_ROPE_HALF && rope_style != SINKATTN_ROPE_INTERLEAVED) ||
+      !std::isfinite(mscale))
+    return SINKATTN_INVALID_ARGUMENT;
+  if (num_tokens == 0) return SINKATTN_OK;
+  if (!qkv || !positions || !slot_mapping || !inv_freq || !q_out || !k_cache || !v_cache)
+    return SINKATTN_INVALID_ARGUMENT;
+  if (!aligned(qkv, 16) || (bias && !aligned(bias, 16)) || !aligned(q_out, 16) ||
+      !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(positions, 4) ||
+      !aligned(slot_mapping, 4))
+    return SINKATTN_INVALID_ARGUMENT;
+  if (static_cast<long long>(num_tokens) * (num_qo_heads + 2 * num_kv_heads) * 4 > 0x7fffffffll)
+    return SINKATTN_UNSUPPORTED;
+  sa::PrologueParams p{};
+  p.qkv = static_cast<const uint16_t *>(qkv);
+  p.bias = static_cast<const uint16_t *>(bias);
+  p.positions = positions;
+  p.slot_mapping = slot_mapping;
+  p.q_out = static_cast<uint16_t *>(q_out);
+  p.k_cache = static_cast<uint16_t *>(k_cache);
+  p.v_cache = static_cast<uint16_t *>(v_cache);
+  for (int i = 0; i < kHeadDim / 2; ++i) {
+    if (!std::isfinite(inv_freq[i])) return SINKATTN_INVALID_ARGUMENT;
+    p.inv_freq[i] = inv_freq[i];
+  }
+  p.mscale = mscale;
+  p.num_tokens = num_tokens;
+  p.num_qo_heads = num_qo_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.num_pages = num_pages;
+  p.interleaved = rope_style == SINKATTN_ROPE_INTERLEAVED;
+  return cuda_status(sa::launch_prologue(p, static_cast<cudaStream_t>(stream)), "prologue launch");
+}
+
 }  // extern "C"

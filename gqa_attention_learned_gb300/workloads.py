@@ -235,3 +235,30 @@ def verify_batch(seed=5, batch=64, q_len=4, num_qo_heads=64, num_kv_heads=8, min
     return dict(name="verify", num_qo_heads=num_qo_heads, num_kv_heads=num_kv_heads,
                 head_dim=HEAD_DIM, scale=0.125, q=q, q_len=q_len, sinks=sinks, tree_mask=masks,
                 max_kv_len=int(max(kv_lens)), **pool)
+
+
+def prologue_batch(seq_lens, start_positions, seed=6, num_qo_heads=64, num_kv_heads=8,
+                   bias=True):
+    """Projection outputs of new tokens for the attention prologue: request r
+    appends seq_lens[r] tokens at positions start_positions[r] .. + len - 1
+    to a shuffled paged pool that already holds its first start_positions[r]
+    tokens.  qkv ~ N(0,1), bias ~ N(0, 0.5) (bf16); slot_mapping gives each
+    new token's page * 16 + offset."""
+    rng = np.random.default_rng(seed)
+    lens = [int(x) for x in seq_lens]
+    starts = [int(x) for x in start_positions]
+    heads = num_qo_heads + 2 * num_kv_heads
+    total = sum(lens)
+    qkv = _bf16(_normal(rng, (total, heads * HEAD_DIM)))
+    b = _bf16(_normal(rng, (heads * HEAD_DIM,), 0.5)) if bias else None
+    pool = paged_pool(rng, [s + n for s, n in zip(starts, lens)], num_kv_heads)
+    table = pool["page_table"].numpy()
+    positions, slots = [], []
+    for r, (s, n) in enumerate(zip(starts, lens)):
+        for p in range(s, s + n):
+            positions.append(p)
+            slots.append(int(table[r, p // PAGE_SIZE]) * PAGE_SIZE + p % PAGE_SIZE)
+    return dict(name="prologue", num_qo_heads=num_qo_heads, num_kv_heads=num_kv_heads,
+                head_dim=HEAD_DIM, qkv=qkv, bias=b,
+                positions=torch.tensor(positions, dtype=torch.int32),
+                slot_mapping=torch.tensor(slots, dtype=torch.int32), **pool)

@@ -202,6 +202,59 @@ SINKATTN_API int sinkattn_prefill_paged(const void *q, const int32_t *cu_seqlens
                            int page_size, void *stream);
 
 /*
+ * Attention prologue ("GPT-OSS on day 0", Perplexity blog, model summary
+ * before section "Attention: GQA with attention sinks": YaRN position
+ * encoding as in DeepSeek-V3, QKV projections with biases as in Qwen 2).
+ *
+ * sinkattn_yarn_table (host only): rotary angular frequencies of the
+ * head_dim / 2 pairs and the magnitude factor, after the YaRN paper (Peng et
+ * al., 2023, "NTK-by-parts" and the attention temperature): pair d has
+ * theta_d = base^(-2d / head_dim) and r_d = original_context * theta_d / (2 pi)
+ * rotations over the original context; with ramp g = clamp((r_d - beta_slow)
+ * / (beta_fast - beta_slow), 0, 1) its frequency is
+ * g * theta_d + (1 - g) * theta_d / factor; mscale = 0.1 ln(factor) + 1.
+ * factor = 1 gives plain rotary frequencies and mscale = 1.  The pages give
+ * no parameter values.
+ *   inv_freq : host float [head_dim / 2] (out);  mscale : host float (out)
+ */
+SINKATTN_API int sinkattn_yarn_table(int head_dim, double base, double factor,
+                        double original_context, double beta_fast, double beta_slow,
+                        float *inv_freq, float *mscale);
+
+/*
+ * sinkattn_qkv_prologue: one pass over the QKV projection output of
+ * num_tokens tokens:
+ *   x = qkv[t] + bias (fp32), split into num_qo_heads q rows, num_kv_heads k
+ *   rows, num_kv_heads v rows of head_dim;
+ *   q and k rows rotated: pair (x1, x2) of pair index i at position p becomes
+ *   (x1 cos(p f_i) - x2 sin(p f_i), x2 cos(p f_i) + x1 sin(p f_i)) * mscale;
+ *   q_out[t] = bf16(rotated q); k and v written (bf16, round to nearest
+ *   even, once) to page slot_mapping[t] / page_size, slot
+ *   slot_mapping[t] % page_size of k_cache / v_cache.
+ *   qkv          : bf16 [num_tokens][(num_qo_heads + 2 num_kv_heads) * head_dim]
+ *   bias         : bf16 [(num_qo_heads + 2 num_kv_heads) * head_dim] or NULL
+ *   positions    : int32 [num_tokens] (exact below 2^24)
+ *   slot_mapping : int32 [num_tokens]; an entry < 0 or at or past
+ *                  num_pages * page_size writes no k/v for that token
+ *   inv_freq     : HOST float [head_dim / 2] (copied into the launch, so the
+ *                  call can be captured in a CUDA graph); mscale as above
+ *   rope_style   : SINKATTN_ROPE_HALF (pairs (i, i + head_dim/2)) or
+ *                  SINKATTN_ROPE_INTERLEAVED (pairs (2i, 2i + 1))
+ *   q_out        : bf16 [num_tokens][num_qo_heads][head_dim]
+ *   k_cache, v_cache : the paged cache (see conventions), num_pages pages
+ * Two tokens mapped to the same slot race (one of them wins).
+ */
+#define SINKATTN_ROPE_HALF 0
+#define SINKATTN_ROPE_INTERLEAVED 1
+
+SINKATTN_API int sinkattn_qkv_prologue(const void *qkv, const void *bias,
+                          const int32_t *positions, const int32_t *slot_mapping,
+                          const float *inv_freq, float mscale, int rope_style,
+                          void *q_out, void *k_cache, void *v_cache,
+                          int num_tokens, int num_qo_heads, int num_kv_heads,
+                          int head_dim, int page_size, int num_pages, void *stream);
+
+/*
  * Decode for callers that cannot allocate device memory.
  *
  * Some callers of this library cannot call cudaMalloc at the point where they

@@ -154,3 +154,39 @@ def test_verify_rejects_on_host(lib):
     assert call(mask=ctypes.c_void_p(0x1004)) == sa.INVALID_ARGUMENT     # misaligned mask
     assert call(q=None) == sa.INVALID_ARGUMENT
     assert call(batch=0) == sa.OK
+
+
+def test_yarn_table_matches_oracle(lib):
+    from oracle import prologue as pro
+    for args in ((64, 150000.0, 32.0, 4096, 32.0, 1.0), (64, 10000.0, 1.0, 2048, 32.0, 1.0),
+                 (64, 500000.0, 8.0, 8192, 16.0, 2.0)):
+        f, m = sa.yarn_table(*args)
+        fo, mo = pro.yarn_inv_freq(*args)
+        assert len(f) == 32
+        np_f = [float(x) for x in f]
+        for a, b in zip(np_f, fo):
+            assert abs(a - b) <= 2 ** -23 * abs(b)          # one float rounding
+        assert abs(m - mo) <= 2 ** -23 * mo
+    with pytest.raises(sa.SinkAttnError):
+        sa.yarn_table(factor=0.5)
+    with pytest.raises(sa.SinkAttnError):
+        sa.yarn_table(beta_fast=1.0, beta_slow=1.0)
+
+
+def test_prologue_rejects_on_host(lib):
+    fake = ctypes.c_void_p(0x1000)
+    freq = (ctypes.c_float * 32)(*([0.5] * 32))
+
+    def call(**kw):
+        a = dict(qkv=fake, bias=None, pos=fake, slots=fake, freq=freq, ms=1.0, style=0, q=fake,
+                 k=fake, v=fake, t=4, hq=8, hkv=1, d=64, page=16, pages=1, stream=None)
+        a.update(kw)
+        return lib.sinkattn_qkv_prologue(*a.values())
+
+    assert call(d=128) == sa.UNSUPPORTED
+    assert call(page=32) == sa.UNSUPPORTED
+    assert call(style=2) == sa.INVALID_ARGUMENT
+    assert call(qkv=ctypes.c_void_p(0x1008)) == sa.INVALID_ARGUMENT
+    assert call(bias=ctypes.c_void_p(0x1004)) == sa.INVALID_ARGUMENT
+    assert call(freq=(ctypes.c_float * 32)(*([float("nan")] * 32))) == sa.INVALID_ARGUMENT
+    assert call(t=0) == sa.OK
