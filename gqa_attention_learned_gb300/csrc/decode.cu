@@ -7,7 +7,10 @@
 // started at -inf, blocks merged by log-sum-exp.
 //
 // Design (GB300, HBM-bound):
-//  * One CTA = one (request, KV head, 8-query-head block, KV chunk).  Its
+//  * One CTA = one (request, KV head, 8-query-head block, KV chunk).  When
+//    the plan has one chunk per request the requests are dispatched heaviest
+//    first (by size class, computed from kv_lens in every CTA) so that the
+//    last wave holds the short ones.  Its
 //    NW warps take the chunk's 16-token pages round-robin, each warp running
 //    its own STAGES-deep TMA pipeline: lane 0 issues two 3-D bulk tensor
 //    copies per page (K and V tile, 2 KB each, 128-byte swizzle) onto the
@@ -38,9 +41,6 @@ namespace {
 
 #ifndef SA_DECODE_NW
 #define SA_DECODE_NW 8          // warps per CTA
-#endif
-#ifndef SA_DECODE_CHUNK_MAJOR
-#define SA_DECODE_CHUNK_MAJOR 0
 #endif
 #ifndef SA_DECODE_STAGES
 #define SA_DECODE_STAGES 3      // pages in flight per warp
@@ -92,25 +92,147 @@ __device__ __forceinline__ long long row_index(const DecodeParams &p, int b, int
   }
 }
 
+constexpr int kBuckets = 8;   // size classes of partial chunks in the dispatch order
+
+// Block-wide exclusive prefix sum of one value per thread; `total` gets the sum.
+__device__ __forceinline__ int block_excl_scan(int v, int *scratch, int &total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  int before = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < kNW; ++w) {
+    const int sw = scratch[w];
+    before += w < warp ? sw : 0;
+    tot += sw;
+  }
+  __syncthreads();
+  total = tot;
+  return before + x - v;
+}
+
+// Chunks of one request under the plan: nfull full chunks and at most one
+// partial last chunk (size class `bucket`).  A request out of range counts as
+// one empty partial chunk (its CTA writes NaN rows).
+struct RequestWork {
+  int nfull, has_part, bucket;
+};
+template <bool kVerify>
+__device__ __forceinline__ RequestWork request_work(const DecodeParams &p, int b) {
+  const int kv_len = p.kv_lens[b];
+  RequestWork r{0, 1, 0};
+  if (request_chunks(kv_len, kVerify ? p.q_len : 0, p.max_pages_per_seq, p.num_splits,
+                     p.pages_per_chunk) == 0)
+    return r;
+  const int pages = ceil_div(kv_len, kPageSize);
+  r.nfull = pages / p.pages_per_chunk;
+  const int part = pages - r.nfull * p.pages_per_chunk;
+  r.has_part = part > 0 || pages == 0;
+  r.bucket = part * kBuckets / p.pages_per_chunk;
+  return r;
+}
+
+// The (request, chunk) of dispatch slot `item`, heaviest first so that the
+// last wave holds the smallest chunks: every full chunk (request order), then
+// the partial last chunks from the largest size class to the smallest
+// (request order within a class).  Every CTA computes the same order from
+// kv_lens with two block scans; false past the last chunk.  (Used for plans
+// with one chunk per request, where this is the requests by size.)
+template <bool kVerify>
+__device__ bool map_item(const DecodeParams &p, int item, int &b_out, int &chunk_out) {
+  __shared__ int scratch[kNW], totals[kBuckets], owner[2];
+  const int per = ceil_div(p.batch, kNW * 32);
+  const int b0 = min(p.batch, static_cast<int>(threadIdx.x) * per);
+  const int b1 = min(p.batch, b0 + per);
+  int nfull = 0, cnt[kBuckets];
+#pragma unroll
+  for (int k = 0; k < kBuckets; ++k) cnt[k] = 0;
+  for (int b = b0; b < b1; ++b) {
+    const RequestWork r = request_work<kVerify>(p, b);
+    nfull += r.nfull;
+#pragma unroll
+    for (int k = 0; k < kBuckets; ++k) cnt[k] += (r.has_part && r.bucket == k) ? 1 : 0;
+  }
+  if (threadIdx.x < kBuckets) totals[threadIdx.x] = 0;
+  if (threadIdx.x == 0) owner[0] = -1;
+  int num_full;
+  const int full_off = block_excl_scan(nfull, scratch, num_full);   // (syncs the zeroing too)
+  if (item < num_full) {
+    if (item >= full_off && item < full_off + nfull) {
+      int acc = full_off;
+      for (int b = b0; b < b1; ++b) {
+        const int nf = request_work<kVerify>(p, b).nfull;
+        if (item < acc + nf) {
+          owner[0] = b;
+          owner[1] = item - acc;
+          break;
+        }
+        acc += nf;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < kBuckets; ++k)
+      if (cnt[k]) atomicAdd(&totals[k], cnt[k]);
+    __syncthreads();
+    int rank = item - num_full, cls = -1;
+    for (int k = kBuckets - 1; k >= 0; --k) {        // uniform over the CTA
+      if (rank < totals[k]) {
+        cls = k;
+        break;
+      }
+      rank -= totals[k];
+    }
+    if (cls >= 0) {
+      int mine = 0;
+#pragma unroll
+      for (int k = 0; k < kBuckets; ++k) mine += k == cls ? cnt[k] : 0;
+      int in_cls;
+      const int off = block_excl_scan(mine, scratch, in_cls);
+      if (rank >= off && rank < off + mine) {
+        int seen = off;
+        for (int b = b0; b < b1; ++b) {
+          const RequestWork r = request_work<kVerify>(p, b);
+          if (r.has_part && r.bucket == cls) {
+            if (seen == rank) {
+              owner[0] = b;
+              owner[1] = r.nfull;
+              break;
+            }
+            ++seen;
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  b_out = owner[0];
+  chunk_out = owner[1];
+  return b_out >= 0;
+}
+
 template <int NB, bool kVerify>
 __global__ void __launch_bounds__(kNW * 32, 2)
 decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
               const DecodeParams p) {
-#if SA_DECODE_CHUNK_MAJOR
-  // chunk-major order: every request's first chunk is dispatched before any
-  // second chunk, so the last wave holds the short trailing chunks
-  const int chunk = blockIdx.z;
-  const int hb = blockIdx.x % p.head_blocks;
-  const int kvh = blockIdx.x / p.head_blocks;
-  const int b = blockIdx.y;
-  const int unit_y = blockIdx.x;
-#else
-  const int chunk = blockIdx.x;
-  const int hb = blockIdx.y % p.head_blocks;
-  const int kvh = blockIdx.y / p.head_blocks;
-  const int b = blockIdx.z;
-  const int unit_y = blockIdx.y;
-#endif
+  // CTA blockIdx.x: (KV head, head block) unit blockIdx.x % U of (request,
+  // chunk) slot blockIdx.x / U.  Plans with one chunk per request and at
+  // most a few waves of CTAs take the requests heaviest first; other plans
+  // take them in order, chunk fastest (their many short CTAs would pay more
+  // for the ordering than it saves).
+  const int units = p.num_kv_heads * p.head_blocks;
+  const int unit_y = static_cast<int>(blockIdx.x % units);
+  const int hb = unit_y % p.head_blocks;
+  const int kvh = unit_y / p.head_blocks;
+  const int slot = static_cast<int>(blockIdx.x / units);
+  int b = slot / p.num_splits, chunk = slot % p.num_splits;
+  if (p.sorted_dispatch && !map_item<kVerify>(p, slot, b, chunk)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   constexpr int kCols = kHeadsPerTile * NB;       // query rows of this CTA
@@ -489,12 +611,10 @@ cudaError_t launch_variant(const CUtensorMap &kmap, const CUtensorMap &vmap, con
   cudaError_t err = cudaFuncSetAttribute(decode_kernel<NB, kVerify>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (err != cudaSuccess) return err;
-#if SA_DECODE_CHUNK_MAJOR
-  dim3 grid(p.num_kv_heads * p.head_blocks, p.batch, p.num_splits);
-#else
-  dim3 grid(p.num_splits, p.num_kv_heads * p.head_blocks, p.batch);
-#endif
-  decode_kernel<NB, kVerify><<<grid, kNW * 32, kSmemBytes, stream>>>(kmap, vmap, p);
+  const unsigned long long ctas =
+      static_cast<unsigned long long>(p.num_splits) * p.batch * p.num_kv_heads * p.head_blocks;
+  if (ctas > 0x7fffffffull) return cudaErrorInvalidConfiguration;
+  decode_kernel<NB, kVerify><<<static_cast<unsigned>(ctas), kNW * 32, kSmemBytes, stream>>>(kmap, vmap, p);
   return cudaGetLastError();
 }
 

@@ -37,6 +37,7 @@ struct DecodeParams {
   int col_blocks;               // 8-row column blocks per CTA (1 or 2)
   int head_blocks;              // CTAs per (request, KV head, chunk) = ceil(rows / (8 col_blocks))
   int num_pages, num_splits, pages_per_chunk;
+  int sorted_dispatch;          // one chunk per request: requests heaviest first
 };
 
 // Column blocks per CTA for q_len * group query rows per KV head.

@@ -22,6 +22,8 @@ constexpr int kMaxDevices = 64;
 constexpr int kMinPagesPerChunk = 16;   // keeps merge traffic under ~3% of KV
 constexpr int kWavesTarget = 4;
 constexpr int kVerifyWavesTarget = 2;
+constexpr int kMaxChunkPages = 512;     // one-chunk plans only up to 8192 tokens
+constexpr int kSortedWaves = 4;         // heaviest-first dispatch up to this many waves
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -112,6 +114,7 @@ struct DecodePlan {
   int pages_per_chunk = 1;
   size_t counters_bytes = 0;  // merge counters (zeroed once, reset by every call)
   size_t workspace_bytes = 0;
+  int sorted_dispatch = 0;    // one chunk per request, <= kSortedWaves waves of CTAs
 };
 
 // CTA column blocks and head blocks of q_len tokens per request (q_len = 1:
@@ -138,7 +141,11 @@ DecodePlan plan_decode(int batch, int q_len, int num_qo_heads, int num_kv_heads,
   } else {
     const long long units = static_cast<long long>(batch) * num_kv_heads * head_blocks;
     const long long slots = static_cast<long long>(std::max(num_sms, 1)) * sa::decode_ctas_per_sm();
-    if (col_blocks == 1) {
+    if (col_blocks == 1 && units >= slots) {
+      // at least a wave of (request, KV head) CTAs: whole requests, which the
+      // kernel dispatches heaviest first, unless a request is very long
+      s = std::max(1, ceil_div(max_pages, kMaxChunkPages));
+    } else if (col_blocks == 1) {
       s = static_cast<int>(std::min<long long>((kWavesTarget * slots + units - 1) / std::max(units, 1ll),
                                                1 << 20));
     } else {
@@ -152,6 +159,11 @@ DecodePlan plan_decode(int batch, int q_len, int num_qo_heads, int num_kv_heads,
   s = std::max(1, std::min({s, sa::decode_max_splits(), max_pages}));
   plan.pages_per_chunk = ceil_div(max_pages, s);
   plan.num_splits = ceil_div(max_pages, plan.pages_per_chunk);
+  {
+    const long long units = static_cast<long long>(batch) * num_kv_heads * head_blocks;
+    const long long slots = static_cast<long long>(std::max(num_sms, 1)) * sa::decode_ctas_per_sm();
+    plan.sorted_dispatch = plan.num_splits == 1 && units <= kSortedWaves * slots;
+  }
   if (plan.num_splits > 1) {
     const size_t units = static_cast<size_t>(batch) * num_kv_heads * head_blocks;
     plan.counters_bytes = (units * sizeof(int) + 255) & ~size_t(255);
@@ -299,6 +311,7 @@ int decode_common(const void *q, const void *k_cache, const void *v_cache,
   p.num_pages = num_pages;
   p.num_splits = plan.num_splits;
   p.pages_per_chunk = plan.pages_per_chunk;
+  p.sorted_dispatch = plan.sorted_dispatch;
   return cuda_status(sa::launch_decode(kmap, vmap, p, static_cast<cudaStream_t>(stream)),
                      "decode launch");
 }
