@@ -41,6 +41,27 @@ DECODE_WORKLOAD = ("gpt-oss-20b decode: 64 q / 8 KV heads, head_dim 64, batch 64
 
 # ----------------------------------------------------------------- helpers
 
+# DRAM bytes (read + write) of one headline decode launch from an ncu capture
+# (profiles/decode_gptoss20b_b64.md), valid only for the kernel sources it was
+# taken on: a change to them reports the traffic as unknown.
+DECODE_TRAFFIC = {"sources_sha256_16": "7fbb3b2abe70d89e", "bytes": 265_304_064}
+DECODE_SOURCES = ("gqa_attention_learned_gb300/csrc/decode.cu",
+                  "gqa_attention_learned_gb300/csrc/kernels.cuh",
+                  "gqa_attention_learned_gb300/csrc/ptx.cuh")
+
+
+def decode_traffic():
+    import hashlib
+    h = hashlib.sha256()
+    try:
+        for f in DECODE_SOURCES:
+            with open(os.path.join(ROOT, f), "rb") as fh:
+                h.update(fh.read())
+    except OSError:
+        return None
+    return DECODE_TRAFFIC["bytes"] if h.hexdigest()[:16] == DECODE_TRAFFIC["sources_sha256_16"] else None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -633,7 +654,7 @@ def gpu_arm(args):
         "roofline": {"bound": "hbm", "achieved": round(kernel_gbps, 2),
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(kernel_gbps / peaks["hbm_gbs"], 4),
-                     "traffic": None, "peak_source": peak_src,
+                     "traffic": decode_traffic(), "peak_source": peak_src,
                      "kernel": "decode_kernel (chunk merge inside the kernel)",
                      "bytes_per_launch": d["nbytes"]},
         "e2e": d["e2e"], "e2e_kv_h2d": d["e2e_kv_h2d"],
