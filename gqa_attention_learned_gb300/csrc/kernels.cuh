@@ -68,7 +68,12 @@ struct PrefillParams {
   int num_qo_heads, num_kv_heads, group;
   int max_pages_per_seq, num_pages;
   int paged;                     // 0: k/v [Tk][Hkv][64], 1: paged cache
-  int num_q_tiles;               // ceil(max_q_len / tile)
+  int num_q_tiles;               // query tiles per (request, head) -- per (request, KV head) when verifying
+  // Verification (paged): every request has max_q_len tokens, the last of
+  // its keys; the query rows of a KV head are its (token, head) pairs, q is
+  // [num_seqs * max_q_len][Hq][64]; tree_mask [num_seqs][max_q_len] or null.
+  int verify;
+  const uint64_t *tree_mask;
 };
 
 cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap,

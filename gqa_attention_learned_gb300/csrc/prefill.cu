@@ -124,29 +124,45 @@ __device__ __forceinline__ void pack_chunk(uint32_t (&r)[32], uint64_t scale2, u
   }
 }
 
-template <bool kPaged>
+template <bool kPaged, bool kVerify>
 __global__ void __launch_bounds__(kThreads, 2)
 prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
-  const int per_tile = p.num_seqs * p.num_qo_heads;
-  const int qt = p.num_q_tiles - 1 - static_cast<int>(blockIdx.x / per_tile);
-  const int rem = static_cast<int>(blockIdx.x % per_tile);
-  const int head = rem % p.num_qo_heads;
-  const int seq = rem / p.num_qo_heads;
-  const int kvh = head / p.group;
+  static_assert(kPaged || !kVerify, "verification reads the paged cache");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint4 nan4 = make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
 
-  // ---- request geometry and argument checks (uniform over the CTA)
-  const int q_start = p.cu_seqlens_q[seq];
-  const int q_end = p.cu_seqlens_q[seq + 1];
-  const int q_len = q_end - q_start;
-  int kv_len, k_start = 0;
-  if constexpr (kPaged) {
+  // ---- work item and request geometry (uniform over the CTA).  Prefill: a
+  // 128-row query tile of one head.  Verification: the query rows of one KV
+  // head of one request, ordered (token, head in group), 128 / group tokens
+  // per tile; every request has q_len tokens, the last q_len of its keys.
+  int seq, kvh, head = 0, qt, q_start, q_len, kv_len, k_start = 0;
+  if constexpr (kVerify) {
+    const int per_tile = p.num_seqs * p.num_kv_heads;
+    qt = static_cast<int>(blockIdx.x / per_tile);
+    const int rem = static_cast<int>(blockIdx.x % per_tile);
+    kvh = rem % p.num_kv_heads;
+    seq = rem / p.num_kv_heads;
+    q_len = p.max_q_len;
+    q_start = seq * q_len;
     kv_len = p.kv_lens[seq];
   } else {
-    k_start = p.cu_seqlens_k[seq];
-    kv_len = p.cu_seqlens_k[seq + 1] - k_start;
+    const int per_tile = p.num_seqs * p.num_qo_heads;
+    qt = p.num_q_tiles - 1 - static_cast<int>(blockIdx.x / per_tile);
+    const int rem = static_cast<int>(blockIdx.x % per_tile);
+    head = rem % p.num_qo_heads;
+    seq = rem / p.num_qo_heads;
+    kvh = head / p.group;
+    q_start = p.cu_seqlens_q[seq];
+    q_len = p.cu_seqlens_q[seq + 1] - q_start;
+    if constexpr (kPaged) {
+      kv_len = p.kv_lens[seq];
+    } else {
+      k_start = p.cu_seqlens_k[seq];
+      kv_len = p.cu_seqlens_k[seq + 1] - k_start;
+    }
   }
+  const int q_end = q_start + q_len;
   bool bad = q_start < 0 || q_len < 0 || q_end > p.total_q || q_len > p.max_q_len ||
              kv_len < q_len || kv_len > p.max_kv_len;
   if constexpr (kPaged) {
@@ -155,25 +171,33 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     bad = bad || k_start < 0 || k_start + kv_len > p.total_k;
   }
   if (bad) {
-    // Poison every row this request owns that lies inside the buffers.
+    // Poison every row this request owns that lies inside the buffers (once:
+    // by the CTA of its first query tile).
     if (qt != 0 || q_start < 0 || q_start >= p.total_q) return;
     const int stop = min(max(q_end, q_start), p.total_q);
-    for (int t = q_start + threadIdx.x; t < stop; t += kThreads) {
-      uint4 nan4 = make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
-      uint4 *dst = reinterpret_cast<uint4 *>(p.out + (static_cast<size_t>(t) * p.num_qo_heads + head) * kHeadDim);
+    const int heads_here = kVerify ? p.group : 1;
+    for (int idx = threadIdx.x; idx < (stop - q_start) * heads_here; idx += kThreads) {
+      const int t = q_start + idx / heads_here;
+      const int h = kVerify ? kvh * p.group + idx % heads_here : head;
+      uint4 *dst = reinterpret_cast<uint4 *>(p.out + (static_cast<size_t>(t) * p.num_qo_heads + h) * kHeadDim);
 #pragma unroll
       for (int i = 0; i < 8; ++i) dst[i] = nan4;
-      if (p.lse) p.lse[static_cast<size_t>(t) * p.num_qo_heads + head] = NAN;
+      if (p.lse) p.lse[static_cast<size_t>(t) * p.num_qo_heads + h] = NAN;
     }
     return;
   }
-  const int i0 = qt * kBM;
+  // first query row (token) of the tile, rows (tokens) in it, query rows used
+  const int tok_per_tile = kVerify ? kBM / p.group : kBM;
+  const int i0 = qt * tok_per_tile;
   if (i0 >= q_len) return;
-  const int rows = min(kBM, q_len - i0);
+  const int rows_tok = min(tok_per_tile, q_len - i0);
+  const int rows = kVerify ? rows_tok * p.group : rows_tok;
   const int shift = kv_len - q_len;                        // bottom-right causal offset
-  const int key_end = shift + i0 + rows;                   // keys needed, exclusive (<= kv_len)
+  const int key_end = shift + i0 + rows_tok;               // keys needed, exclusive (<= kv_len)
   const int n_tiles = cdiv(key_end, kBN);
   const int npages = cdiv(kv_len, kPageSize);
+  // softmax threads with a query row (verification tiles may be partly empty)
+  const int live_threads = kVerify ? min(kBM, 32 * cdiv(rows, 32)) : kBM;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -198,8 +222,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       mbar_init(&bar.v_empty[s], 1);
     }
     mbar_init(&bar.s_full, 1);
-    mbar_init(&bar.s_free, kBM);
-    mbar_init(&bar.p_full, kBM);
+    mbar_init(&bar.s_free, live_threads);
+    mbar_init(&bar.p_full, live_threads);
     mbar_init(&bar.pv_done, 1);
     mbar_init(&bar.o_final, 1);
     bar.bad = 0;
@@ -248,7 +272,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       tma_prefetch_desc(&kmap);
       tma_prefetch_desc(&vmap);
       mbar_arrive_expect_tx(&bar.q_full, kBM * kHeadDim * 2);
-      tma_load_3d(sQ, &qmap, &bar.q_full, 0, head, q_start + i0);
+      if constexpr (kVerify)   // box {64, group, 128 / group}: rows (token, head)
+        tma_load_3d(sQ, &qmap, &bar.q_full, 0, kvh * p.group, q_start + i0);
+      else
+        tma_load_3d(sQ, &qmap, &bar.q_full, 0, head, q_start + i0);
     }
     const uint32_t tS = tmem + kColS;
     const uint64_t dq = umma_desc_sw128(smem_u32(sQ), 16, 1024);
@@ -318,8 +345,18 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     // ------------------------------------------------------------- softmax
     const int r = threadIdx.x;                          // row = TMEM lane
     const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const int i = i0 + r;
-    const int limit = min(shift + i + 1, kv_len);       // keys [0, limit) visible
+    // token (within the request) and head of this thread's query row
+    const int i = kVerify ? i0 + r / p.group : i0 + r;
+    const int row_head = kVerify ? kvh * p.group + r % p.group : head;
+    const bool tree = kVerify && p.tree_mask != nullptr;
+    // keys [0, limit) are candidates (causal); with a draft tree, key
+    // draft0 + u is visible only if bit u of the row's mask is set
+    const int limit = tree ? kv_len : min(shift + i + 1, kv_len);
+    const int draft0 = shift;
+    uint64_t vis = 0;
+    if constexpr (kVerify) {
+      if (tree && r < rows) vis = p.tree_mask[static_cast<size_t>(seq) * q_len + i];
+    }
     const float sl2 = p.scale_log2;
     const bool pos_scale = sl2 >= 0.f;
     // Masked scores are replaced (by index, so NaN keys cannot leak) with the
@@ -330,12 +367,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     // only moves when a row max exceeds it by more than kRescaleLog2, at which
     // point O and d are rescaled; out = O/d and lse = m + log2(d) are exact
     // for any reference, and P stays below 2^kRescaleLog2.
-    float m = p.sinks[head] * kLog2e;
+    float m = p.sinks[row_head] * kLog2e;
     float d = 1.f;
     bool ok = true;
     uint32_t x[4][32];
 
-    for (int j = 0; j < n_tiles; ++j) {
+    const bool live = warp * 32 < live_threads;         // warp-uniform
+    for (int j = 0; live && j < n_tiles; ++j) {
       // warp-uniform: the tcgen05.ld/st below are .sync.aligned
       if (!__all_sync(0xffffffffu, mbar_wait(&bar.s_full, j & 1))) { ok = false; break; }
       tc_fence_after();
@@ -354,6 +392,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
 #pragma unroll
           for (int e = 0; e < 32; ++e)
             if (k0 + 32 * c + e >= limit) x[c][e] = masked_raw;
+      }
+      if (tree && __any_sync(0xffffffffu, k0 + kBN > draft0)) {   // tiles holding draft keys
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int u = k0 + 32 * c + e - draft0;
+            if (u >= 0 && u < 64 && !((vis >> u) & 1)) x[c][e] = masked_raw;
+          }
       }
       float mx;
       if (pos_scale) {
@@ -426,7 +473,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       tc_fence_before();
       mbar_arrive(&bar.p_full);
     }
-    if (__all_sync(0xffffffffu, mbar_wait(&bar.o_final, 0))) {
+    if (!live) {
+      // no query rows in this warp: nothing to read
+    } else if (__all_sync(0xffffffffu, mbar_wait(&bar.o_final, 0))) {
       tc_fence_after();
       if (ok && n_tiles > 0) {
         tmem_ld32(trow + kColO, x[0]);
@@ -443,7 +492,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     __syncthreads();
     const bool failed = bar.bad != 0;
     if (r < rows) {
-      const size_t row = static_cast<size_t>(q_start + i) * p.num_qo_heads + head;
+      const size_t row = static_cast<size_t>(q_start + i) * p.num_qo_heads + row_head;
       const float inv = d > 0.f ? 1.f / d : 0.f;
       uint4 *dst = reinterpret_cast<uint4 *>(p.out + row * kHeadDim);
       auto o = [&](int c) { return __uint_as_float(x[c >> 5][c & 31]) * inv; };
@@ -451,7 +500,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       for (int c = 0; c < kHeadDim / 8; ++c) {
         uint4 w;
         if (failed) {
-          w = make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
+          w = nan4;
         } else {
           w.x = pack_bf16(o(8 * c + 0), o(8 * c + 1));
           w.y = pack_bf16(o(8 * c + 2), o(8 * c + 3));
@@ -477,26 +526,27 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
 
 }  // namespace
 
+template <bool kPaged, bool kVerify>
+static cudaError_t launch_prefill_variant(const CUtensorMap &qmap, const CUtensorMap &kmap,
+                           const CUtensorMap &vmap, const PrefillParams &p, unsigned ctas,
+                           cudaStream_t stream) {
+  cudaError_t err = cudaFuncSetAttribute(prefill_kernel<kPaged, kVerify>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (err != cudaSuccess) return err;
+  prefill_kernel<kPaged, kVerify><<<ctas, kThreads, kSmemBytes, stream>>>(qmap, kmap, vmap, p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap,
                            const CUtensorMap &vmap, const PrefillParams &p, cudaStream_t stream) {
   static_assert(kSmemBytes <= 113 * 1024, "two CTAs per SM");
-  const unsigned long long ctas =
-      static_cast<unsigned long long>(p.num_q_tiles) * p.num_seqs * p.num_qo_heads;
+  const unsigned long long ctas = static_cast<unsigned long long>(p.num_q_tiles) * p.num_seqs *
+                                  (p.verify ? p.num_kv_heads : p.num_qo_heads);
   if (ctas == 0) return cudaSuccess;
   if (ctas > 0x7fffffffull) return cudaErrorInvalidConfiguration;
-  cudaError_t err;
-  if (p.paged) {
-    err = cudaFuncSetAttribute(prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kSmemBytes);
-    if (err != cudaSuccess) return err;
-    prefill_kernel<true><<<static_cast<unsigned>(ctas), kThreads, kSmemBytes, stream>>>(qmap, kmap, vmap, p);
-  } else {
-    err = cudaFuncSetAttribute(prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kSmemBytes);
-    if (err != cudaSuccess) return err;
-    prefill_kernel<false><<<static_cast<unsigned>(ctas), kThreads, kSmemBytes, stream>>>(qmap, kmap, vmap, p);
-  }
-  return cudaGetLastError();
+  if (p.verify) return launch_prefill_variant<true, true>(qmap, kmap, vmap, p, static_cast<unsigned>(ctas), stream);
+  if (p.paged) return launch_prefill_variant<true, false>(qmap, kmap, vmap, p, static_cast<unsigned>(ctas), stream);
+  return launch_prefill_variant<false, false>(qmap, kmap, vmap, p, static_cast<unsigned>(ctas), stream);
 }
 
 }  // namespace sa

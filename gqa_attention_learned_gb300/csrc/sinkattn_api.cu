@@ -115,7 +115,20 @@ struct DecodePlan {
   size_t counters_bytes = 0;  // merge counters (zeroed once, reset by every call)
   size_t workspace_bytes = 0;
   int sorted_dispatch = 0;    // one chunk per request, <= kSortedWaves waves of CTAs
+  int tensor_cores = 0;       // verification on the tcgen05 kernel (no KV split)
 };
+
+// Verification of q_len tokens runs on the tensor-core (tcgen05) kernel when
+// the query rows of a KV head fill a good part of its 128-row tile (at least
+// 3 blocks of 8), the group divides 128, no request is longer than one
+// chunk's limit, and the launch has a wave of CTAs without splitting the KV.
+bool verify_on_tensor_cores(int batch, int q_len, int num_qo_heads, int num_kv_heads,
+                            int max_pages, int num_sms) {
+  const int group = num_qo_heads / num_kv_heads;
+  if (q_len < 2 || 128 % group || q_len * group < 24 || max_pages > kMaxChunkPages) return false;
+  const long long tiles = ceil_div(q_len, 128 / group);
+  return tiles * batch * num_kv_heads >= 2ll * std::max(num_sms, 1);
+}
 
 // CTA column blocks and head blocks of q_len tokens per request (q_len = 1:
 // plain decode, one 8-row column block per CTA).
@@ -135,6 +148,12 @@ DecodePlan plan_decode(int batch, int q_len, int num_qo_heads, int num_kv_heads,
   int col_blocks, head_blocks;
   decode_blocks(q_len, group, &col_blocks, &head_blocks);
   const int max_pages = std::max(1, ceil_div(max_kv_len, kPageSize));
+  if (requested == 0 &&
+      verify_on_tensor_cores(batch, q_len, num_qo_heads, num_kv_heads, max_pages, num_sms)) {
+    plan.tensor_cores = 1;
+    plan.pages_per_chunk = max_pages;
+    return plan;
+  }
   int s;
   if (requested > 0) {
     s = requested;
@@ -153,6 +172,7 @@ DecodePlan plan_decode(int batch, int q_len, int num_qo_heads, int num_kv_heads,
       // makes the kernel throughput-bound: fewer, longer chunks (measured)
       s = static_cast<int>(std::min<long long>(kVerifyWavesTarget * slots / std::max(units, 1ll),
                                                1 << 20));
+      s = std::max(s, ceil_div(max_pages, kMaxChunkPages));
     }
     s = std::min(s, std::max(1, max_pages / kMinPagesPerChunk));
   }
@@ -276,6 +296,40 @@ int decode_common(const void *q, const void *k_cache, const void *v_cache,
   if (plan.num_splits > 1) {
     if (!workspace || workspace_bytes < plan.workspace_bytes) return SINKATTN_WORKSPACE_TOO_SMALL;
     if (!aligned(workspace, 256)) return SINKATTN_INVALID_ARGUMENT;
+  }
+
+  if (plan.tensor_cores) {
+    // query rows (token, head) of a KV head: box {64, group, 128 / group}
+    CUtensorMap qmap, kmap, vmap;
+    const unsigned long long rows = static_cast<unsigned long long>(num_kv_heads) * kPageSize;
+    if (!encode_map(&qmap, q, num_qo_heads, static_cast<unsigned long long>(batch) * q_len, group,
+                    kPrefillTile / group) ||
+        !encode_map(&kmap, k_cache, rows, num_pages, kPageSize, 1) ||
+        !encode_map(&vmap, v_cache, rows, num_pages, kPageSize, 1))
+      return fail_msg("cuTensorMapEncodeTiled failed");
+    sa::PrefillParams pp{};
+    pp.q = static_cast<const uint16_t *>(q);
+    pp.page_table = page_table;
+    pp.kv_lens = kv_lens;
+    pp.sinks = sinks;
+    pp.out = static_cast<uint16_t *>(out);
+    pp.lse = lse;
+    pp.scale_log2 = scale * sa::kLog2e;
+    pp.num_seqs = batch;
+    pp.total_q = batch * q_len;
+    pp.max_q_len = q_len;
+    pp.max_kv_len = max_kv_len;
+    pp.num_qo_heads = num_qo_heads;
+    pp.num_kv_heads = num_kv_heads;
+    pp.group = group;
+    pp.max_pages_per_seq = max_pages_per_seq;
+    pp.num_pages = num_pages;
+    pp.paged = 1;
+    pp.num_q_tiles = ceil_div(q_len, kPrefillTile / group);
+    pp.verify = 1;
+    pp.tree_mask = tree_mask;
+    return cuda_status(sa::launch_prefill(qmap, kmap, vmap, pp, static_cast<cudaStream_t>(stream)),
+                       "verification launch");
   }
 
   CUtensorMap kmap, vmap;

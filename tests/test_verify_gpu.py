@@ -116,3 +116,48 @@ def test_rows_that_see_no_key_and_short_requests():
     assert torch.equal(out[0, 1].float(), torch.zeros(8, 64))
     sinks = w["sinks"]
     assert torch.equal(torch.isinf(lse[0, 1]), torch.isinf(sinks))
+
+
+# ---------------------------------------------------- tensor-core (tcgen05) route
+# With at least a wave of (request, KV head) CTAs and >= 24 query rows per KV
+# head, sinkattn_verify runs the tcgen05 kernel (rows = (token, head) pairs of
+# a KV head in one 128-row tile, no KV split); the plan reports one split and
+# no workspace for it.
+
+def _tc_batch(q_len, hq, hkv):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    tiles = -(-q_len // (128 // (hq // hkv)))
+    return -(-2 * sms // (hkv * tiles)) + 2
+
+
+@pytest.mark.parametrize("q_len,hq,hkv,tree", [(4, 64, 8, False), (8, 64, 8, True),
+                                               (16, 64, 8, True), (32, 64, 8, True),
+                                               (6, 32, 8, False), (2, 32, 2, True)])
+def test_tensor_core_route(q_len, hq, hkv, tree):
+    b = _tc_batch(q_len, hq, hkv)
+    w = workloads.verify_batch(seed=300 + q_len + hq, batch=b, q_len=q_len, num_qo_heads=hq,
+                               num_kv_heads=hkv, max_len=180, tree=tree)
+    assert sa.verify_plan(b, q_len, hq, hkv, w["max_kv_len"]) == (1, 0)
+    out, lse = run_verify(w)
+    ro, rl = ref_verify(w)
+    assert_out_close(out, ro)
+    assert_lse_close(lse, rl)
+
+
+def test_tensor_core_route_matches_split_kernel_and_poisons_short_requests():
+    q_len, hq, hkv = 8, 64, 8
+    b = _tc_batch(q_len, hq, hkv)
+    w = workloads.verify_batch(seed=17, batch=b, q_len=q_len, max_len=700, tree=True)
+    lens = w["kv_lens"].clone()
+    lens[3] = q_len - 1                      # fewer keys than new tokens
+    w["kv_lens"] = lens
+    tc_out, tc_lse = run_verify(w)                    # tensor-core route
+    mma_out, mma_lse = run_verify(w, num_splits=1)    # split-KV route
+    assert torch.isnan(tc_out[3].float()).all() and torch.isnan(tc_lse[3]).all()
+    assert torch.isnan(mma_out[3].float()).all()
+    ok = [i for i in range(b) if i != 3]
+    reqs = ok[:6] + ok[-4:]
+    ro, rl = ref_verify(w, reqs)
+    for o, l in ((tc_out, tc_lse), (mma_out, mma_lse)):
+        assert_out_close(o[reqs], ro)
+        assert_lse_close(l[reqs], rl)
