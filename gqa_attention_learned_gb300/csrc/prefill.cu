@@ -124,6 +124,91 @@ __device__ __forceinline__ void pack_chunk(uint32_t (&r)[32], uint64_t scale2, u
   }
 }
 
+// Block-wide exclusive prefix sum of one value per thread (kThreads
+// threads); `total` gets the sum.
+__device__ __forceinline__ int block_excl_scan(int v, int *scratch, int &total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  int before = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < kThreads / 32; ++w) {
+    const int sw = scratch[w];
+    before += w < warp ? sw : 0;
+    tot += sw;
+  }
+  __syncthreads();
+  total = tot;
+  return before + x - v;
+}
+
+// Request of dispatch slot `slot` with the requests heaviest first: 8 size
+// classes of ceil(kv_len / 16) pages (largest first), request order within a
+// class.  Every CTA derives the same order from kv_lens (a reduction and a
+// block scan), so the last wave holds the short requests.
+__device__ int request_by_size(const PrefillParams &p, int slot) {
+  constexpr int kClasses = 8;
+  __shared__ int scratch[kThreads / 32], totals[kClasses], owner;
+  const int max_pages = max(1, cdiv(p.max_kv_len, kPageSize));
+  auto size_class = [&](int b) {
+    const int pages = cdiv(max(p.kv_lens[b], 0), kPageSize);
+    return min(kClasses - 1, static_cast<int>(static_cast<long long>(pages) * kClasses / (max_pages + 1)));
+  };
+  const int per = cdiv(p.num_seqs, kThreads);
+  const int b0 = min(p.num_seqs, static_cast<int>(threadIdx.x) * per);
+  const int b1 = min(p.num_seqs, b0 + per);
+  int cnt[kClasses];
+#pragma unroll
+  for (int k = 0; k < kClasses; ++k) cnt[k] = 0;
+  for (int b = b0; b < b1; ++b) {
+    const int c = size_class(b);
+#pragma unroll
+    for (int k = 0; k < kClasses; ++k) cnt[k] += c == k ? 1 : 0;
+  }
+  if (threadIdx.x < kClasses) totals[threadIdx.x] = 0;
+  if (threadIdx.x == 0) owner = -1;
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < kClasses; ++k)
+    if (cnt[k]) atomicAdd(&totals[k], cnt[k]);
+  __syncthreads();
+  int rank = slot, cls = -1;
+  for (int k = kClasses - 1; k >= 0; --k) {          // uniform over the CTA
+    if (rank < totals[k]) {
+      cls = k;
+      break;
+    }
+    rank -= totals[k];
+  }
+  if (cls >= 0) {
+    int mine = 0;
+#pragma unroll
+    for (int k = 0; k < kClasses; ++k) mine += k == cls ? cnt[k] : 0;
+    int in_cls;
+    const int off = block_excl_scan(mine, scratch, in_cls);
+    if (rank >= off && rank < off + mine) {
+      int seen = off;
+      for (int b = b0; b < b1; ++b) {
+        if (size_class(b) == cls) {
+          if (seen == rank) {
+            owner = b;
+            break;
+          }
+          ++seen;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  return owner;
+}
+
 template <bool kPaged, bool kVerify>
 __global__ void __launch_bounds__(kThreads, 2)
 prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
@@ -138,11 +223,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
   // per tile; every request has q_len tokens, the last q_len of its keys.
   int seq, kvh, head = 0, qt, q_start, q_len, kv_len, k_start = 0;
   if constexpr (kVerify) {
-    const int per_tile = p.num_seqs * p.num_kv_heads;
-    qt = static_cast<int>(blockIdx.x / per_tile);
-    const int rem = static_cast<int>(blockIdx.x % per_tile);
-    kvh = rem % p.num_kv_heads;
-    seq = rem / p.num_kv_heads;
+    // blockIdx: request slot (heaviest first), then KV head, then query tile
+    const int per_req = p.num_kv_heads * p.num_q_tiles;
+    const int rem = static_cast<int>(blockIdx.x % per_req);
+    qt = rem % p.num_q_tiles;
+    kvh = rem / p.num_q_tiles;
+    seq = request_by_size(p, static_cast<int>(blockIdx.x / per_req));
+    if (seq < 0) return;
     q_len = p.max_q_len;
     q_start = seq * q_len;
     kv_len = p.kv_lens[seq];
