@@ -79,33 +79,6 @@ constexpr uint32_t kIdescPV = umma_idesc_bf16(128, 64, false, true);
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
-// 2^x on the FMA pipe, for the share of the softmax exponentials that the
-// MUFU unit does not take.  Range reduction x = n + f with n = round(x) (the
-// 1.5 * 2^23 shifter leaves n in the low mantissa bits of t), f in [-1/2, 1/2];
-// 2^f by a cubic with minimax relative error 7.5e-5 (Remez exchange, see
-// gen_exp2_poly.py), far below bf16's 2^-9 rounding of P; 2^n is added to
-// the exponent field.  Inputs below -125 are clamped there (result ~2e-38,
-// i.e. 0 next to any unmasked term) so the exponent sum stays a normal number.
-#ifndef SA_POLY_NUM
-#define SA_POLY_NUM 0        // SA_POLY_NUM of every 8 exponentials use the polynomial
-#endif
-constexpr float kP0 = 0.99992806f, kP1 = 0.69326097f, kP2 = 0.24261113f, kP3 = 0.05517167f;
-
-__device__ __forceinline__ float exp2_poly(float x) {
-  x = fmaxf(x, -125.f);
-  const float t = x + 12582912.f;
-  const float n = t - 12582912.f;
-  const float f = x - n;
-  const float p = fmaf(fmaf(fmaf(kP3, f, kP2), f, kP1), f, kP0);
-  return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
-}
-
-template <int E>
-__device__ __forceinline__ float exp2_mixed(float x) {
-  if constexpr ((E & 7) < SA_POLY_NUM) return exp2_poly(x);
-  else return ex2(x);
-}
-
 // P = 2^(s * sl2 - mu) for 32 scores, packed as bf16 pairs into r[0..15];
 // the pair sums accumulate in `acc` (fp32x2).
 template <int E = 0>
@@ -116,8 +89,8 @@ __device__ __forceinline__ void pack_chunk(uint32_t (&r)[32], uint64_t scale2, u
     f2_unpack(f2_fma(f2_pack(__uint_as_float(r[2 * E]), __uint_as_float(r[2 * E + 1])), scale2,
                      negmu2),
               x0, x1);
-    const float p0 = exp2_mixed<2 * E>(x0);
-    const float p1 = exp2_mixed<2 * E + 1>(x1);
+    const float p0 = ex2(x0);
+    const float p1 = ex2(x1);
     acc = f2_add(acc, f2_pack(p0, p1));
     r[E] = pack_bf16(p0, p1);
     pack_chunk<E + 1>(r, scale2, negmu2, acc);

@@ -219,7 +219,7 @@ const char *sinkattn_status_string(int status) {
   }
 }
 
-int sinkattn_version(void) { return 100; }
+int sinkattn_version(void) { return 200; }   // 0.2.0: verification, prologue, YaRN table
 
 const char *sinkattn_last_error(void) { return g_last_error; }
 
