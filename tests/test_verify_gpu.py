@@ -161,3 +161,16 @@ def test_tensor_core_route_matches_split_kernel_and_poisons_short_requests():
     for o, l in ((tc_out, tc_lse), (mma_out, mma_lse)):
         assert_out_close(o[reqs], ro)
         assert_lse_close(l[reqs], rl)
+
+
+def test_tensor_core_route_large_batch():
+    """400 requests over one KV head on the tensor-core route: the CTAs rank
+    the requests by size with several requests per thread."""
+    w = workloads.verify_batch(seed=19, batch=400, q_len=4, num_qo_heads=8, num_kv_heads=1,
+                               max_len=300, tree=True)
+    assert sa.verify_plan(400, 4, 8, 1, w["max_kv_len"]) == (1, 0)
+    out, lse = run_verify(w)
+    reqs = list(range(0, 400, 7))
+    ro, rl = ref_verify(w, reqs)
+    assert_out_close(out[reqs], ro)
+    assert_lse_close(lse[reqs], rl)
