@@ -146,6 +146,12 @@ SINKATTN_API int sinkattn_decode(const void *q, const void *k_cache, const void 
  *   other arguments, the split plan (sinkattn_verify_plan) and the workspace
  *   rules: as for sinkattn_decode.  kv_len < q_len makes the request's rows
  *   NaN.  q_len = 1 with tree_mask = NULL computes what sinkattn_decode does.
+ * Kernel choice (host-side sizes only, so a plan can be reused): with
+ * num_splits = 0, at least 24 query rows per KV head (q_len times the group
+ * size, which must divide 128), max_kv_len <= 8192 and enough (request, KV
+ * head) pairs to fill the GPU once, the rows of a KV head run on the tensor
+ * cores (tcgen05) in one pass over its keys; the plan then reports one split
+ * and no workspace.  Otherwise the split-KV kernel of sinkattn_decode runs.
  */
 #define SINKATTN_MAX_VERIFY_TOKENS 64
 
