@@ -271,29 +271,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     tmem_alloc(&bar.tmem_base, kTmemCols);
     tmem_relinquish();
   }
-  if (threadIdx.x == kProducerWarp * 32) {
-    mbar_init(&bar.q_full, 1);
-    for (int s = 0; s < kKStages; ++s) {
-      mbar_init(&bar.k_full[s], 1);
-      mbar_init(&bar.k_empty[s], 1);
-    }
-    for (int s = 0; s < kVStages; ++s) {
-      mbar_init(&bar.v_full[s], 1);
-      mbar_init(&bar.v_empty[s], 1);
-    }
-    mbar_init(&bar.s_full, 1);
-    mbar_init(&bar.s_free, live_threads);
-    mbar_init(&bar.p_full, live_threads);
-    mbar_init(&bar.pv_done, 1);
-    mbar_init(&bar.o_final, 1);
-    bar.bad = 0;
-    fence_mbar_init();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = bar.tmem_base;
-
   const int32_t *table = kPaged ? p.page_table + static_cast<size_t>(seq) * p.max_pages_per_seq : nullptr;
   // K (t = 0) or V (t = 1) of tile j into its ring slot, once the slot is free
   auto load = [&](int j, int t) -> bool {
@@ -326,17 +303,45 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     return true;
   };
   if (warp == kProducerWarp) {
-    // ------------------------------------------- loads and QK^T (one thread)
+    // barriers, then the loads the first S needs (Q and the first K tiles),
+    // before the CTA-wide barrier: their latency runs under the tensor-memory
+    // allocation and the barrier
     if (lane == 0) {
+      mbar_init(&bar.q_full, 1);
+      for (int s = 0; s < kKStages; ++s) {
+        mbar_init(&bar.k_full[s], 1);
+        mbar_init(&bar.k_empty[s], 1);
+      }
+      for (int s = 0; s < kVStages; ++s) {
+        mbar_init(&bar.v_full[s], 1);
+        mbar_init(&bar.v_empty[s], 1);
+      }
+      mbar_init(&bar.s_full, 1);
+      mbar_init(&bar.s_free, live_threads);
+      mbar_init(&bar.p_full, live_threads);
+      mbar_init(&bar.pv_done, 1);
+      mbar_init(&bar.o_final, 1);
+      bar.bad = 0;
+      fence_mbar_init();
       tma_prefetch_desc(&qmap);
       tma_prefetch_desc(&kmap);
       tma_prefetch_desc(&vmap);
       mbar_arrive_expect_tx(&bar.q_full, kBM * kHeadDim * 2);
       if constexpr (kVerify)   // box {64, group, 128 / group}: rows (token, head)
-        tma_load_3d(sQ, &qmap, &bar.q_full, 0, kvh * p.group, q_start + i0);
+        tma_load_3d(smem + kOffQ, &qmap, &bar.q_full, 0, kvh * p.group, q_start + i0);
       else
-        tma_load_3d(sQ, &qmap, &bar.q_full, 0, head, q_start + i0);
+        tma_load_3d(smem + kOffQ, &qmap, &bar.q_full, 0, head, q_start + i0);
     }
+    __syncwarp();
+    for (int j = 0; j < min(n_tiles, kKStages); ++j) load(j, 0);   // fresh slots: no waits
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bar.tmem_base;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------- loads and QK^T (one thread)
     const uint32_t tS = tmem + kColS;
     const uint64_t dq = umma_desc_sw128(smem_u32(sQ), 16, 1024);
     auto issue_qk = [&](int j) -> bool {
@@ -354,8 +359,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       __syncwarp();
       return true;
     };
-    bool ok = true;
-    for (int j = 0; ok && j < min(n_tiles, kKStages); ++j) ok = load(j, 0);
+    bool ok = true;                 // Q and the first K tiles are on their way
     ok = ok && __all_sync(0xffffffffu, mbar_wait(&bar.q_full, 0)) && issue_qk(0);
     for (int j = 0; ok && j + 1 < n_tiles; ++j) {
       // S of tile j has been read: compute S of tile j+1 during this softmax
