@@ -608,8 +608,7 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
 template <int NB, bool kVerify>
 cudaError_t launch_variant(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParams &p,
                            cudaStream_t stream) {
-  cudaError_t err = cudaFuncSetAttribute(decode_kernel<NB, kVerify>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  cudaError_t err = set_smem_once<decode_kernel<NB, kVerify>>(kSmemBytes);
   if (err != cudaSuccess) return err;
   const unsigned long long ctas =
       static_cast<unsigned long long>(p.num_splits) * p.batch * p.num_kv_heads * p.head_blocks;

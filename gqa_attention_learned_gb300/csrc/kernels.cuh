@@ -2,6 +2,7 @@
 // kernel translation units.  Not installed; no torch types anywhere.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda.h>
@@ -10,6 +11,22 @@
 namespace sa {
 
 constexpr int kHeadDim = 64;
+
+// Sets a kernel's dynamic shared memory limit once per device (the attribute
+// belongs to the function on the current device); later calls are free.  One
+// flag set per kernel: the kernel itself is the template argument.
+template <auto kernel>
+inline cudaError_t set_smem_once(int bytes) {
+  static std::atomic<unsigned long long> done{0};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (err == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return err;
+}
 constexpr int kPageSize = 16;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;

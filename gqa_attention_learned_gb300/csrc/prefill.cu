@@ -594,8 +594,7 @@ template <bool kPaged, bool kVerify>
 static cudaError_t launch_prefill_variant(const CUtensorMap &qmap, const CUtensorMap &kmap,
                            const CUtensorMap &vmap, const PrefillParams &p, unsigned ctas,
                            cudaStream_t stream) {
-  cudaError_t err = cudaFuncSetAttribute(prefill_kernel<kPaged, kVerify>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  cudaError_t err = set_smem_once<prefill_kernel<kPaged, kVerify>>(kSmemBytes);
   if (err != cudaSuccess) return err;
   prefill_kernel<kPaged, kVerify><<<ctas, kThreads, kSmemBytes, stream>>>(qmap, kmap, vmap, p);
   return cudaGetLastError();
