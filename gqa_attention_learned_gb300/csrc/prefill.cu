@@ -272,8 +272,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     tmem_relinquish();
   }
   const int32_t *table = kPaged ? p.page_table + static_cast<size_t>(seq) * p.max_pages_per_seq : nullptr;
-  // K (t = 0) or V (t = 1) of tile j into its ring slot, once the slot is free
-  auto load = [&](int j, int t) -> bool {
+  // paged: the page id of this lane's 16 keys of tile j (lanes 0..7), else -1
+  auto page_of = [&](int j) -> int {
+    const int pg = j * (kBN / kPageSize) + lane;
+    return kPaged && lane < kBN / kPageSize && pg < npages ? table[pg] : -1;
+  };
+  // K (t = 0) or V (t = 1) of tile j into its ring slot, once the slot is
+  // free; paged tiles use the page ids `pid` (from page_of, read ahead of time
+  // by the issuing warps so the table's latency stays off their loop)
+  auto load_with = [&](int j, int t, int pid) -> bool {
     const int ns = t == 0 ? kKStages : kVStages;
     const int s = j % ns;
     uint64_t *full = t == 0 ? &bar.k_full[s] : &bar.v_full[s];
@@ -285,8 +292,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     if constexpr (kPaged) {
       // lanes 0..7 each own one 16-token page of the 128-key tile
       const int pg = j * (kBN / kPageSize) + lane;
-      int pid = -1;
-      if (lane < kBN / kPageSize && pg < npages) pid = table[pg];
       const bool ok = pid >= 0 && pid < p.num_pages;
       if (t == 0 && lane < kBN / kPageSize && pg < npages && !ok) atomicOr(&bar.bad, 1);
       const unsigned mask = __ballot_sync(0xffffffffu, ok);
@@ -302,6 +307,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     __syncwarp();
     return true;
   };
+  auto load = [&](int j, int t) -> bool { return load_with(j, t, page_of(j)); };
+
   if (warp == kProducerWarp) {
     // barriers, then the loads the first S needs (Q and the first K tiles),
     // before the CTA-wide barrier: their latency runs under the tensor-memory
@@ -360,13 +367,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       return true;
     };
     bool ok = true;                 // Q and the first K tiles are on their way
+    int pk = page_of(kKStages);     // ids of the next K tile to load
     ok = ok && __all_sync(0xffffffffu, mbar_wait(&bar.q_full, 0)) && issue_qk(0);
     for (int j = 0; ok && j + 1 < n_tiles; ++j) {
       // S of tile j has been read: compute S of tile j+1 during this softmax
       if (!__all_sync(0xffffffffu, mbar_wait(&bar.s_free, j & 1))) { ok = false; break; }
       tc_fence_after();
-      ok = issue_qk(j + 1) &&
-           (j + kKStages >= n_tiles || load(j + kKStages, 0));    // K slot freed by QK^T of tile j
+      ok = issue_qk(j + 1);
+      if (ok && j + kKStages < n_tiles) {             // K slot freed by QK^T of tile j
+        ok = load_with(j + kKStages, 0, pk);
+        pk = page_of(j + kKStages + 1);
+      }
     }
     if (!ok && lane == 0) atomicOr(&bar.bad, 1);
   } else if (warp == kMmaWarp) {
@@ -374,6 +385,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const uint32_t tP = tmem + kColP, tO = tmem + kColO;
     bool ok = true;
     for (int j = 0; ok && j < min(n_tiles, kVStages); ++j) ok = load(j, 1);
+    int pv_ids = page_of(kVStages);    // ids of the next V tile to load
     for (int j = 0; ok && j < n_tiles; ++j) {
       const int s = j % kVStages;
       if (!__all_sync(0xffffffffu, mbar_wait(&bar.p_full, j & 1)) ||
@@ -400,7 +412,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       }
       __syncwarp();
       // V of tile j+2 into the slot this P V reads, once it has finished
-      if (j + kVStages < n_tiles && !load(j + kVStages, 1)) { ok = false; break; }
+      if (j + kVStages < n_tiles) {
+        if (!load_with(j + kVStages, 1, pv_ids)) { ok = false; break; }
+        pv_ids = page_of(j + kVStages + 1);
+      }
     }
     if (!ok && lane == 0) atomicOr(&bar.bad, 1);
     if (lane == 0) umma_commit(&bar.o_final);
