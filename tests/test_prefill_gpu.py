@@ -172,3 +172,26 @@ def test_extend_bad_requests():
     ro, rl = ref_extend(sub)
     assert_out_close(out[:10], ro)
     assert_lse_close(lse[:10], rl)
+
+
+def test_long_sequence_sampled_rows():
+    """One 20,000-token sequence (157 query tiles, up to 157 KV tiles per
+    CTA): sampled rows, including the last ones, against the oracle."""
+    w = workloads.custom_prefill([20000], seed=31, num_qo_heads=8, num_kv_heads=1,
+                                 special_sinks=True)
+    out, lse = run_prefill(w)
+    rows = [0, 1, 127, 128, 5000, 12345, 19871, 19872, 19998, 19999]
+    ro, rl = ref_prefill(w, rows=rows)
+    assert_out_close(out[rows], ro[rows])
+    assert_lse_close(lse[rows], rl[rows])
+
+
+def test_extend_on_long_prefix_sampled_rows():
+    """Chunked prefill of 256 tokens after a 30,000-token paged prefix."""
+    w = workloads.extend_batch([256, 40], [30000, 12000], seed=12, num_qo_heads=8,
+                               num_kv_heads=2)
+    out, lse = run_extend(w)
+    rows = [0, 1, 127, 128, 255, 256, 295]
+    ro, rl = ref_extend(w, rows=rows)
+    assert_out_close(out[rows], ro[rows])
+    assert_lse_close(lse[rows], rl[rows])
