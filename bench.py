@@ -639,6 +639,7 @@ def gpu_arm(args):
     dist_init("nccl" if world > 1 else "gloo")
     import gqa_attention_learned_gb300 as sa
     sa.load()
+    sa.set_programmatic_launch(not args.plain_launch)
     peaks, peak_src = load_peaks()
 
     sections = set(args.sections.split(","))
@@ -668,6 +669,9 @@ def gpu_arm(args):
                    "num_kv_heads": 8, "head_dim": 64, "page_size": 16,
                    "kv_tokens": sum(int(x) for x in d["w"]["kv_lens"]),
                    "num_splits": d["splits"],
+                   "launch": "plain" if args.plain_launch else
+                             "programmatic dependent launch (a decode ranks its requests and "
+                             "reads its first page ids while the previous kernel drains)",
                    "l2": "inputs larger than L2: two KV pool copies (2 x 671 MB) alternate"},
         "pct_of_hbm_peak": round(100 * d["gbps"] / peaks["hbm_gbs"], 2),
         "roofline": {"bound": "hbm", "achieved": round(kernel_gbps, 2),
@@ -805,6 +809,8 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline decode only")
     ap.add_argument("--sections", default="graph,long,verify,prologue,prefill,mixed",
                     help="extra sections after the headline decode")
+    ap.add_argument("--plain-launch", action="store_true",
+                    help="launch decode kernels without programmatic dependent launch")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--oracle-worker", default=None, help=argparse.SUPPRESS)

@@ -23,6 +23,7 @@ SIGNATURES = {
     "sinkattn_status_string": (ctypes.c_char_p, [_c_int]),
     "sinkattn_version": (_c_int, []),
     "sinkattn_last_error": (ctypes.c_char_p, []),
+    "sinkattn_set_programmatic_launch": (_c_int, [_c_int]),
     "sinkattn_decode_plan": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                       ctypes.POINTER(_c_int), ctypes.POINTER(_c_size)]),
     "sinkattn_decode": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _vp, _c_float, _vp, _vp,
@@ -82,6 +83,14 @@ def load():
 
 def status_string(status):
     return load().sinkattn_status_string(int(status)).decode()
+
+
+def set_programmatic_launch(enable):
+    """Process-wide switch for programmatic dependent launch of the decode
+    kernel (decode, decode_static_scratch, split-KV verify); returns the
+    previous setting.  While on, kv_lens and page_table of a call must not be
+    written by the kernel launched just before it on the stream."""
+    return bool(load().sinkattn_set_programmatic_launch(1 if enable else 0))
 
 
 def _check(fn, status):

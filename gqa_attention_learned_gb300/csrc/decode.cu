@@ -92,129 +92,106 @@ __device__ __forceinline__ long long row_index(const DecodeParams &p, int b, int
   }
 }
 
-constexpr int kBuckets = 8;   // size classes of partial chunks in the dispatch order
+constexpr int kBuckets = 8;   // size classes of shorter requests in the dispatch order
 
-// Block-wide exclusive prefix sum of one value per thread; `total` gets the sum.
-__device__ __forceinline__ int block_excl_scan(int v, int *scratch, int &total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) scratch[warp] = x;
-  __syncthreads();
-  int before = 0, tot = 0;
-#pragma unroll
-  for (int w = 0; w < kNW; ++w) {
-    const int sw = scratch[w];
-    before += w < warp ? sw : 0;
-    tot += sw;
-  }
-  __syncthreads();
-  total = tot;
-  return before + x - v;
-}
-
-// Chunks of one request under the plan: nfull full chunks and at most one
-// partial last chunk (size class `bucket`).  A request out of range counts as
-// one empty partial chunk (its CTA writes NaN rows).
-struct RequestWork {
-  int nfull, has_part, bucket;
-};
+// Size class of a request in plans with one chunk per request (no division:
+// `per_page` = kBuckets / pages_per_chunk): requests as long as the chunk
+// limit in the top class kBuckets, shorter ones in classes 0..kBuckets-1 by
+// page count; empty and out-of-range requests in class 0.  Every CTA
+// evaluates the same instructions on the same lengths, so all agree.
 template <bool kVerify>
-__device__ __forceinline__ RequestWork request_work(const DecodeParams &p, int b) {
-  const int kv_len = p.kv_lens[b];
-  RequestWork r{0, 1, 0};
-  if (request_chunks(kv_len, kVerify ? p.q_len : 0, p.max_pages_per_seq, p.num_splits,
-                     p.pages_per_chunk) == 0)
-    return r;
+__device__ __forceinline__ int size_class(const DecodeParams &p, int kv_len, float per_page) {
   const int pages = ceil_div(kv_len, kPageSize);
-  r.nfull = pages / p.pages_per_chunk;
-  const int part = pages - r.nfull * p.pages_per_chunk;
-  r.has_part = part > 0 || pages == 0;
-  r.bucket = part * kBuckets / p.pages_per_chunk;
-  return r;
+  if (kv_len < (kVerify ? p.q_len : 0) || pages > p.max_pages_per_seq ||
+      pages > p.pages_per_chunk)
+    return 0;
+  if (pages == p.pages_per_chunk) return kBuckets;
+  return min(kBuckets - 1, __float2int_rz(static_cast<float>(pages) * per_page));
 }
 
-// The (request, chunk) of dispatch slot `item`, heaviest first so that the
-// last wave holds the smallest chunks: every full chunk (request order), then
-// the partial last chunks from the largest size class to the smallest
-// (request order within a class).  Every CTA computes the same order from
-// kv_lens with two block scans; false past the last chunk.  (Used for plans
-// with one chunk per request, where this is the requests by size.)
+// The request of dispatch slot `item` for plans with one chunk per request,
+// heaviest first so that the last wave holds the short requests: size class
+// descending, request order within a class.  Every warp derives the same
+// order from kv_lens on its own (no block barrier): class counts of each
+// group of 32 requests come from two warp reductions of 6-bit fields, the
+// request from one ballot per group.  Returns -1 past the last request;
+// `kv_len` gets the request's length.
 template <bool kVerify>
-__device__ bool map_item(const DecodeParams &p, int item, int &b_out, int &chunk_out) {
-  __shared__ int scratch[kNW], totals[kBuckets], owner[2];
-  const int per = ceil_div(p.batch, kNW * 32);
-  const int b0 = min(p.batch, static_cast<int>(threadIdx.x) * per);
-  const int b1 = min(p.batch, b0 + per);
-  int nfull = 0, cnt[kBuckets];
+__device__ int request_by_size(const DecodeParams &p, int item, int &kv_len) {
+  constexpr int kClasses = kBuckets + 1;
+  constexpr int kLow = 5;                       // classes 0..4 in the first word, 5..8 in the second
+  static_assert(kClasses <= 2 * kLow, "two words of 6-bit counters");
+  constexpr int kHeld = 8;                      // groups of 32 requests kept in registers
+  const int lane = threadIdx.x & 31;
+  const int groups = ceil_div(p.batch, 32);
+  const float per_page = static_cast<float>(kBuckets) / static_cast<float>(p.pages_per_chunk);
+  int len[kHeld], cls_of[kHeld];
 #pragma unroll
-  for (int k = 0; k < kBuckets; ++k) cnt[k] = 0;
-  for (int b = b0; b < b1; ++b) {
-    const RequestWork r = request_work<kVerify>(p, b);
-    nfull += r.nfull;
-#pragma unroll
-    for (int k = 0; k < kBuckets; ++k) cnt[k] += (r.has_part && r.bucket == k) ? 1 : 0;
+  for (int u = 0; u < kHeld; ++u) {
+    const int b = u * 32 + lane;
+    len[u] = u < groups && b < p.batch ? __ldg(p.kv_lens + b) : 0;
   }
-  if (threadIdx.x < kBuckets) totals[threadIdx.x] = 0;
-  if (threadIdx.x == 0) owner[0] = -1;
-  int num_full;
-  const int full_off = block_excl_scan(nfull, scratch, num_full);   // (syncs the zeroing too)
-  if (item < num_full) {
-    if (item >= full_off && item < full_off + nfull) {
-      int acc = full_off;
-      for (int b = b0; b < b1; ++b) {
-        const int nf = request_work<kVerify>(p, b).nfull;
-        if (item < acc + nf) {
-          owner[0] = b;
-          owner[1] = item - acc;
-          break;
-        }
-        acc += nf;
-      }
-    }
-  } else {
+  auto group_class = [&](int u, int &l) {
+    const int b = u * 32 + lane;
+    l = 0;
+    int c = -1;
 #pragma unroll
-    for (int k = 0; k < kBuckets; ++k)
-      if (cnt[k]) atomicAdd(&totals[k], cnt[k]);
-    __syncthreads();
-    int rank = item - num_full, cls = -1;
-    for (int k = kBuckets - 1; k >= 0; --k) {        // uniform over the CTA
-      if (rank < totals[k]) {
-        cls = k;
-        break;
+    for (int v = 0; v < kHeld; ++v)
+      if (v == u) {
+        l = len[v];
+        c = cls_of[v];
       }
-      rank -= totals[k];
+    if (u >= kHeld) {
+      l = b < p.batch ? __ldg(p.kv_lens + b) : 0;
+      c = b < p.batch ? size_class<kVerify>(p, l, per_page) : -1;
     }
-    if (cls >= 0) {
-      int mine = 0;
+    return c;
+  };
+  unsigned lo = 0, hi = 0;                      // class counts, 6 bits each (a group adds <= 32)
+  int total[kClasses];
 #pragma unroll
-      for (int k = 0; k < kBuckets; ++k) mine += k == cls ? cnt[k] : 0;
-      int in_cls;
-      const int off = block_excl_scan(mine, scratch, in_cls);
-      if (rank >= off && rank < off + mine) {
-        int seen = off;
-        for (int b = b0; b < b1; ++b) {
-          const RequestWork r = request_work<kVerify>(p, b);
-          if (r.has_part && r.bucket == cls) {
-            if (seen == rank) {
-              owner[0] = b;
-              owner[1] = r.nfull;
-              break;
-            }
-            ++seen;
-          }
-        }
-      }
+  for (int k = 0; k < kClasses; ++k) total[k] = 0;
+  for (int u = 0; u < groups; ++u) {
+    const int b = u * 32 + lane;
+    int l = 0;
+#pragma unroll
+    for (int v = 0; v < kHeld; ++v)
+      if (v == u) l = len[v];
+    if (u >= kHeld) l = b < p.batch ? __ldg(p.kv_lens + b) : 0;
+    const int c = b < p.batch ? size_class<kVerify>(p, l, per_page) : -1;
+#pragma unroll
+    for (int v = 0; v < kHeld; ++v)
+      if (v == u) cls_of[v] = c;
+    lo = c >= 0 && c < kLow ? 1u << (6 * c) : 0u;
+    hi = c >= kLow ? 1u << (6 * (c - kLow)) : 0u;
+    lo = __reduce_add_sync(0xffffffffu, lo);
+    hi = __reduce_add_sync(0xffffffffu, hi);
+#pragma unroll
+    for (int k = 0; k < kClasses; ++k)
+      total[k] += static_cast<int>(((k < kLow ? lo : hi) >> (6 * (k < kLow ? k : k - kLow))) & 63u);
+  }
+  int rank = item, cls = -1;
+#pragma unroll
+  for (int k = kClasses - 1; k >= 0; --k) {
+    if (cls < 0) {
+      if (rank < total[k]) cls = k;
+      else rank -= total[k];
     }
   }
-  __syncthreads();
-  b_out = owner[0];
-  chunk_out = owner[1];
-  return b_out >= 0;
+  if (cls < 0) return -1;
+  for (int u = 0; u < groups; ++u) {
+    int l;
+    const int c = group_class(u, l);
+    const unsigned hit = __ballot_sync(0xffffffffu, c == cls);
+    const int n = __popc(hit);
+    if (rank < n) {
+      const int src = static_cast<int>(__fns(hit, 0, rank + 1));
+      kv_len = __shfl_sync(0xffffffffu, l, src);
+      return u * 32 + src;
+    }
+    rank -= n;
+  }
+  return -1;                                    // not reached: the classes cover the batch
 }
 
 template <int NB, bool kVerify>
@@ -232,12 +209,18 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
   const int kvh = unit_y / p.head_blocks;
   const int slot = static_cast<int>(blockIdx.x / units);
   int b = slot / p.num_splits, chunk = slot % p.num_splits;
-  if (p.sorted_dispatch && !map_item<kVerify>(p, slot, b, chunk)) return;
+  int kv_len;
+  if (p.sorted_dispatch) {                 // one chunk per request
+    b = request_by_size<kVerify>(p, slot, kv_len);
+    chunk = 0;
+    if (b < 0) return;
+  } else {
+    kv_len = p.kv_lens[b];
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   constexpr int kCols = kHeadsPerTile * NB;       // query rows of this CTA
 
-  const int kv_len = p.kv_lens[b];
   // verification needs its q_len tokens among the keys; plain decode allows kv_len = 0
   const int nchunks = request_chunks(kv_len, kVerify ? p.q_len : 0, p.max_pages_per_seq,
                                      p.num_splits, p.pages_per_chunk);
@@ -271,6 +254,19 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
     }
   }
   __syncwarp();
+
+  // Page ids of this warp's pages, 32 at a time (lane j holds page j of the batch).
+  auto load_ids = [&](int base) -> int {
+    const int j = base + lane;
+    return j < n_my ? table[first + j * kNW] : -1;
+  };
+  int ids_cur = load_ids(0), ids_next = load_ids(32);
+
+  // Up to here only kv_lens and page_table were read; everything below may
+  // depend on the previous kernel on the stream (q, the caches, sinks, masks,
+  // the outputs and the workspace).
+  grid_dependency_wait();
+  launch_dependents();
 
   // Q^T as the B operand: lane (g, t) holds row g of each column block, dims
   // 16ks+2t.. and 16ks+8+2t..
@@ -320,12 +316,6 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
 #pragma unroll
     for (int i = 0; i < 4; ++i) o[nb][i][0] = o[nb][i][1] = o[nb][i][2] = o[nb][i][3] = 0.f;
 
-  // Page ids of this warp's pages, 32 at a time (lane j holds page j of the batch).
-  auto load_ids = [&](int base) -> int {
-    const int j = base + lane;
-    return j < n_my ? table[first + j * kNW] : -1;
-  };
-  int ids_cur = load_ids(0), ids_next = load_ids(32);
   bool lane_bad = false;     // meaningful on lane 0
 
   auto issue = [&](int j) {  // all lanes call; lane 0 issues
@@ -613,8 +603,8 @@ cudaError_t launch_variant(const CUtensorMap &kmap, const CUtensorMap &vmap, con
   const unsigned long long ctas =
       static_cast<unsigned long long>(p.num_splits) * p.batch * p.num_kv_heads * p.head_blocks;
   if (ctas > 0x7fffffffull) return cudaErrorInvalidConfiguration;
-  decode_kernel<NB, kVerify><<<static_cast<unsigned>(ctas), kNW * 32, kSmemBytes, stream>>>(kmap, vmap, p);
-  return cudaGetLastError();
+  return launch_kernel(decode_kernel<NB, kVerify>, static_cast<unsigned>(ctas), kNW * 32,
+                       kSmemBytes, stream, programmatic_launch(), kmap, vmap, p);
 }
 
 }  // namespace

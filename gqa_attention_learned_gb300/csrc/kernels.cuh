@@ -3,6 +3,7 @@
 #pragma once
 
 #include <atomic>
+#include <utility>
 #include <cstddef>
 #include <cstdint>
 #include <cuda.h>
@@ -27,6 +28,30 @@ inline cudaError_t set_smem_once(int bytes) {
   if (err == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
   return err;
 }
+// Process-wide switch: decode and verification kernels launched with the
+// programmatic-serialization attribute (see sinkattn_set_programmatic_launch).
+bool programmatic_launch();
+
+// Launches `kernel` on `stream`; with `programmatic` the launch may start while
+// the previous kernel on the stream is still running (the kernel orders its
+// dependent reads and writes after grid_dependency_wait).
+template <typename... Params, typename... Args>
+inline cudaError_t launch_kernel(void (*kernel)(Params...), unsigned grid, unsigned block,
+                                 int smem, cudaStream_t stream, bool programmatic,
+                                 Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = programmatic ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 constexpr int kPageSize = 16;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;

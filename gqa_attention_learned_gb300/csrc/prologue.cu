@@ -47,6 +47,10 @@ template <int kTok>                // tokens per CTA
 __global__ void __launch_bounds__(kThreads)
 prologue_kernel(const __grid_constant__ PrologueParams p) {
   __shared__ float2 cs[kTok][kPairs];          // (cos, sin) * mscale
+  // A decode launched programmatically after this kernel may start its
+  // request ranking now; it waits for this grid to finish before reading q
+  // or the caches.
+  launch_dependents();
   const int tok0 = blockIdx.x * kTok;
   for (int j = threadIdx.x; j < kTok * kPairs; j += kThreads) {
     const int tt = j / kPairs, i = j % kPairs;

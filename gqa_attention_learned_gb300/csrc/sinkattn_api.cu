@@ -204,6 +204,9 @@ size_t decode_counter_bytes(int batch, int num_qo_heads, int num_kv_heads, int q
   const size_t units = static_cast<size_t>(batch) * num_kv_heads * head_blocks;
   return (units * sizeof(int) + 255) & ~size_t(255);
 }
+std::atomic<int> g_programmatic{0};
+bool programmatic_launch() { return g_programmatic.load(std::memory_order_relaxed) != 0; }
+
 }  // namespace sa
 
 extern "C" {
@@ -219,7 +222,11 @@ const char *sinkattn_status_string(int status) {
   }
 }
 
-int sinkattn_version(void) { return 200; }   // 0.2.0: verification, prologue, YaRN table
+int sinkattn_version(void) { return 300; }   // 0.3.0: programmatic dependent launch
+
+int sinkattn_set_programmatic_launch(int enable) {
+  return sa::g_programmatic.exchange(enable != 0 ? 1 : 0);
+}
 
 const char *sinkattn_last_error(void) { return g_last_error; }
 

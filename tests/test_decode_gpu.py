@@ -188,7 +188,8 @@ def test_decode_on_side_stream_and_no_lse():
 
 def test_large_batch_heaviest_first_dispatch():
     """600 requests over one KV head: the plan keeps whole requests and the
-    CTAs rank them by size (several requests per thread of the ranking)."""
+    CTAs rank them by size (more groups of 32 lengths than a warp keeps in
+    registers, empty requests among them)."""
     w = workloads.decode_batch(seed=77, batch=600, num_qo_heads=8, num_kv_heads=1, min_len=0,
                                max_len=700)
     assert sa.decode_plan(600, 8, 1, w["max_kv_len"]) == (1, 0)
