@@ -87,8 +87,8 @@ def status_string(status):
 
 def set_programmatic_launch(enable):
     """Process-wide switch for programmatic dependent launch of the decode
-    kernel (decode, decode_static_scratch, split-KV verify); returns the
-    previous setting.  While on, kv_lens and page_table of a call must not be
+    and verification kernels (decode, decode_static_scratch, verify); returns
+    the previous setting.  While on, kv_lens and page_table of a call must not be
     written by the kernel launched just before it on the stream."""
     return bool(load().sinkattn_set_programmatic_launch(1 if enable else 0))
 

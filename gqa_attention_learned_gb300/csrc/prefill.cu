@@ -234,6 +234,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     // Poison every row this request owns that lies inside the buffers (once:
     // by the CTA of its first query tile).
     if (qt != 0 || q_start < 0 || q_start >= p.total_q) return;
+    if constexpr (kVerify) grid_dependency_wait();
     const int stop = min(max(q_end, q_start), p.total_q);
     const int heads_here = kVerify ? p.group : 1;
     for (int idx = threadIdx.x; idx < (stop - q_start) * heads_here; idx += kThreads) {
@@ -270,6 +271,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
   if (warp == kMmaWarp) {
     tmem_alloc(&bar.tmem_base, kTmemCols);
     tmem_relinquish();
+  }
+  // Up to here only the metadata was read (cu_seqlens, kv_lens; the page
+  // table below); q, the caches and the outputs may belong to the previous
+  // kernel on the stream (verification launches programmatically).
+  if (kVerify && warp != kProducerWarp) {
+    grid_dependency_wait();
+    launch_dependents();
   }
   const int32_t *table = kPaged ? p.page_table + static_cast<size_t>(seq) * p.max_pages_per_seq : nullptr;
   // paged: the page id of this lane's 16 keys of tile j (lanes 0..7), else -1
@@ -333,6 +341,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       tma_prefetch_desc(&qmap);
       tma_prefetch_desc(&kmap);
       tma_prefetch_desc(&vmap);
+    }
+    // verification: the first K tiles' page ids before waiting for the
+    // previous kernel (prefill is launched plainly and reads them on demand)
+    int first_ids[kKStages];
+#pragma unroll
+    for (int j = 0; j < kKStages; ++j) first_ids[j] = kVerify ? page_of(j) : 0;
+    if constexpr (kVerify) {
+      grid_dependency_wait();
+      launch_dependents();
+    }
+    if (lane == 0) {
       mbar_arrive_expect_tx(&bar.q_full, kBM * kHeadDim * 2);
       if constexpr (kVerify)   // box {64, group, 128 / group}: rows (token, head)
         tma_load_3d(smem + kOffQ, &qmap, &bar.q_full, 0, kvh * p.group, q_start + i0);
@@ -340,7 +359,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         tma_load_3d(smem + kOffQ, &qmap, &bar.q_full, 0, head, q_start + i0);
     }
     __syncwarp();
-    for (int j = 0; j < min(n_tiles, kKStages); ++j) load(j, 0);   // fresh slots: no waits
+    for (int j = 0; j < min(n_tiles, kKStages); ++j) {              // fresh slots: no waits
+      int pid = 0;
+      if constexpr (kVerify) {
+#pragma unroll
+        for (int u = 0; u < kKStages; ++u)
+          if (u == j) pid = first_ids[u];
+      } else {
+        pid = page_of(j);
+      }
+      load_with(j, 0, pid);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -611,8 +640,9 @@ static cudaError_t launch_prefill_variant(const CUtensorMap &qmap, const CUtenso
                            cudaStream_t stream) {
   cudaError_t err = set_smem_once<prefill_kernel<kPaged, kVerify>>(kSmemBytes);
   if (err != cudaSuccess) return err;
-  prefill_kernel<kPaged, kVerify><<<ctas, kThreads, kSmemBytes, stream>>>(qmap, kmap, vmap, p);
-  return cudaGetLastError();
+  // verification follows the decode kernel's launch mode; prefill launches plainly
+  return launch_kernel(prefill_kernel<kPaged, kVerify>, ctas, kThreads, kSmemBytes, stream,
+                       kVerify && programmatic_launch(), qmap, kmap, vmap, p);
 }
 
 cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap,

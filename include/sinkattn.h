@@ -76,15 +76,18 @@ SINKATTN_API const char *sinkattn_last_error(void);
 SINKATTN_API int sinkattn_version(void);
 
 /*
- * Programmatic dependent launch of the decode kernel (the kernel of
- * sinkattn_decode, sinkattn_decode_static_scratch and the split-KV route of
- * sinkattn_verify).  Process-wide, off by default; returns the previous
- * setting.  When on, that kernel may be scheduled while the kernel launched
- * before it on the same stream is still running: its CTAs rank the requests
- * (kv_lens) and read their first page ids (page_table), then wait for the
+ * Programmatic dependent launch of the decode and verification kernels
+ * (sinkattn_decode, sinkattn_decode_static_scratch and both routes of
+ * sinkattn_verify; prefill is unaffected).  Process-wide, off by default;
+ * returns the previous setting.  When on, such a kernel may be scheduled
+ * while the kernel launched before it on the same stream is still running:
+ * its CTAs rank the requests (kv_lens), read their first page ids
+ * (page_table) and set up shared and tensor memory, then wait for the
  * earlier kernel to finish before they read q, the caches, sinks or
  * tree_mask and before they write out, lse or the workspace; they let the
- * next kernel on the stream be scheduled only after that wait.
+ * next kernel on the stream be scheduled only after that wait.  The
+ * prologue kernel (sinkattn_qkv_prologue) lets such a kernel be scheduled
+ * as soon as all of its own CTAs have started.
  * Caller's contract while it is on: kv_lens and page_table of a call are not
  * written by the kernel launched immediately before the call on its stream
  * (they may come from host copies, memsets or any earlier kernel).  Launches

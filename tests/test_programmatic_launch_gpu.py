@@ -1,12 +1,13 @@
-"""Programmatic dependent launch of the decode kernel.
+"""Programmatic dependent launch of the decode and verification kernels.
 
-With the switch on, a decode may be scheduled while the kernel before it on
-the stream still runs: it ranks its requests and reads its first page ids
-(kv_lens, page_table), then waits for that kernel before touching q, the
-caches or its outputs.  These tests chain kernels whose outputs feed the next
-decode (decode -> decode through q, prologue -> decode through q and the
-cache) and check that every result equals the one of the same calls made one
-at a time with the switch off, bit for bit, and the float64 oracle.
+With the switch on, a decode or verification may be scheduled while the
+kernel before it on the stream still runs: it ranks its requests and reads its
+first page ids (kv_lens, page_table), then waits for that kernel before
+touching q, the caches or its outputs.  These tests chain kernels whose
+outputs feed the next call (decode -> decode and verify -> verify through q,
+prologue -> decode through q and the cache) and check that every result
+equals the one of the same calls made one at a time with the switch off, bit
+for bit, and the float64 oracle.
 """
 
 import numpy as np
@@ -223,3 +224,43 @@ def test_programmatic_chain_in_a_cuda_graph():
                               d["sinks"], d["scale"], d["max_kv_len"], want_lse=False)
             torch.cuda.synchronize()
         assert torch.equal(out2.view(torch.int16), e2.view(torch.int16))
+
+
+@pytest.mark.parametrize("q_len,tree", [(2, False), (4, False), (8, True)])
+def test_verify_chain_through_q(q_len, tree):
+    """Verification outputs feed the next verification's q ([B, q_len, Hq,
+    64] both).  2 tokens (16 rows per KV head) take the split-KV kernel, 4
+    and 8 the tensor-core kernel; both launch programmatically."""
+    w = workloads.verify_batch(seed=40 + q_len, batch=64, q_len=q_len, max_len=1200, tree=tree)
+    d = _dev(w)
+    mask = d.get("tree_mask")
+
+    def run(sync_each):
+        q, outs, lses = d["q"], [], []
+        for _ in range(5):
+            out = torch.full_like(q, float("nan"))
+            lse = torch.full(q.shape[:3], float("nan"), dtype=torch.float32, device=DEV)
+            sa.verify(q, d["k_cache"], d["v_cache"], d["page_table"], d["kv_lens"], d["sinks"],
+                      d["scale"], d["max_kv_len"], tree_mask=mask, out=out, lse=lse)
+            if sync_each:
+                torch.cuda.synchronize()
+            outs.append(out)
+            lses.append(lse)
+            q = out
+        torch.cuda.synchronize()
+        return outs, lses
+
+    with programmatic(True):
+        fast, fast_lse = run(False)
+    with programmatic(False):
+        slow, slow_lse = run(True)
+    for a, b, la, lb in zip(fast, slow, fast_lse, slow_lse):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+        assert torch.equal(la, lb)
+    m = w.get("tree_mask")
+    ro, rl = oracle.verify(to_np(w["q"]), Bf16Pool(w["k_cache"]), Bf16Pool(w["v_cache"]),
+                           w["page_table"].numpy(), w["kv_lens"].numpy(),
+                           w["sinks"].numpy().astype(np.float64), w["scale"],
+                           tree_mask=None if m is None else m.numpy())
+    assert_out_close(fast[0].cpu(), ro)
+    assert_lse_close(fast_lse[0].cpu(), rl)
