@@ -6,6 +6,7 @@ device memory and the current stream.  There is no fallback: if the shared
 library is missing or fails to load, every call raises.
 """
 
+import contextlib
 import ctypes
 import os
 
@@ -99,16 +100,39 @@ def _check(fn, status):
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
+
+
+def _on(dev):
+    """Makes `dev` the current device for a call (no-op when it already is)."""
+    if dev.index is None or dev.index == torch.cuda.current_device():
+        return contextlib.nullcontext()
+    return torch.cuda.device(dev)
+
+
+_plans = {}
+
+
+def _plan(fn, *args):
+    """fn(*args) for the current device, memoised: plans depend only on
+    host-side sizes and the device's SM count."""
+    key = (fn.__name__, torch.cuda.current_device()) + args
+    hit = _plans.get(key)
+    if hit is None:
+        hit = _plans[key] = fn(*args)
+    return hit
 
 
 def _stream(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+    return stream.cuda_stream
 
 
 def _want(t, name, dtype, dims=None, device=None):
+    if (isinstance(t, torch.Tensor) and t.dtype == dtype and (dims is None or t.dim() == dims)
+            and t.is_cuda and (device is None or t.device == device) and t.is_contiguous()):
+        return
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.dtype != dtype:
@@ -155,13 +179,13 @@ def decode(q, k_cache, v_cache, page_table, kv_lens, sinks, scale, max_kv_len, *
         out = torch.empty_like(q)
     if lse is None and want_lse:
         lse = torch.empty(batch, hq, dtype=torch.float32, device=dev)
-    splits, ws_bytes = decode_plan(batch, hq, hkv, max_kv_len, num_splits, head_dim=d,
-                                   page_size=page) if batch else (1, 0)
-    if workspace is None and ws_bytes:
-        # zero-filled once; decode leaves it ready for the next call
-        workspace = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
-    ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    with torch.cuda.device(dev):
+    with _on(dev):
+        splits, ws_bytes = _plan(decode_plan, batch, hq, hkv, int(max_kv_len), int(num_splits),
+                                 0, d, page) if batch else (1, 0)
+        if workspace is None and ws_bytes:
+            # zero-filled once; decode leaves it ready for the next call
+            workspace = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+        ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
         _check("sinkattn_decode", load().sinkattn_decode(
             _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table), page_table.shape[1],
             _ptr(kv_lens), _ptr(sinks), float(scale), _ptr(out), _ptr(lse), batch, hq, hkv, d,
@@ -206,12 +230,12 @@ def verify(q, k_cache, v_cache, page_table, kv_lens, sinks, scale, max_kv_len, *
         out = torch.empty_like(q)
     if lse is None and want_lse:
         lse = torch.empty(batch, q_len, hq, dtype=torch.float32, device=dev)
-    splits, ws_bytes = verify_plan(batch, q_len, hq, hkv, max_kv_len, num_splits, head_dim=d,
-                                   page_size=page) if batch else (1, 0)
-    if workspace is None and ws_bytes:
-        workspace = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
-    ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    with torch.cuda.device(dev):
+    with _on(dev):
+        splits, ws_bytes = _plan(verify_plan, batch, q_len, hq, hkv, int(max_kv_len),
+                                 int(num_splits), 0, d, page) if batch else (1, 0)
+        if workspace is None and ws_bytes:
+            workspace = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+        ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
         _check("sinkattn_verify", load().sinkattn_verify(
             _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table), page_table.shape[1],
             _ptr(kv_lens), _ptr(tree_mask), _ptr(sinks), float(scale), _ptr(out), _ptr(lse), batch,
@@ -238,7 +262,7 @@ def prefill(q, k, v, cu_seqlens, sinks, scale, max_seqlen, *, out=None, lse=None
         out = torch.empty_like(q)
     if lse is None and want_lse:
         lse = torch.empty(total, hq, dtype=torch.float32, device=dev)
-    with torch.cuda.device(dev):
+    with _on(dev):
         _check("sinkattn_prefill", load().sinkattn_prefill(
             _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), cu_seqlens.numel() - 1, total,
             int(max_seqlen), _ptr(sinks), float(scale), _ptr(out), _ptr(lse), hq, hkv, d,
@@ -263,7 +287,7 @@ def prefill_paged(q, cu_seqlens_q, k_cache, v_cache, page_table, kv_lens, sinks,
         out = torch.empty_like(q)
     if lse is None and want_lse:
         lse = torch.empty(total, hq, dtype=torch.float32, device=dev)
-    with torch.cuda.device(dev):
+    with _on(dev):
         _check("sinkattn_prefill_paged", load().sinkattn_prefill_paged(
             _ptr(q), _ptr(cu_seqlens_q), cu_seqlens_q.numel() - 1, total, int(max_q_len),
             _ptr(k_cache), _ptr(v_cache), _ptr(page_table), page_table.shape[1], _ptr(kv_lens),
@@ -292,7 +316,7 @@ def decode_static_scratch(q, k_cache, v_cache, page_table, kv_lens, sinks, scale
         out = torch.empty_like(q)
     if lse is None and want_lse:
         lse = torch.empty(batch, hq, dtype=torch.float32, device=dev)
-    with torch.cuda.device(dev):
+    with _on(dev):
         _check("sinkattn_decode_static_scratch", load().sinkattn_decode_static_scratch(
             _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table), page_table.shape[1],
             _ptr(kv_lens), _ptr(sinks), float(scale), _ptr(out), _ptr(lse), batch, hq, hkv, d,
@@ -334,7 +358,7 @@ def qkv_prologue(qkv, bias, positions, slot_mapping, inv_freq, mscale, k_cache, 
     freq = (_c_float * (d // 2))(*[float(x) for x in inv_freq])
     if q_out is None:
         q_out = torch.empty(tokens, num_qo_heads, d, dtype=torch.bfloat16, device=dev)
-    with torch.cuda.device(dev):
+    with _on(dev):
         _check("sinkattn_qkv_prologue", load().sinkattn_qkv_prologue(
             _ptr(qkv), _ptr(bias), _ptr(positions), _ptr(slot_mapping), freq, float(mscale),
             int(rope_style), _ptr(q_out), _ptr(k_cache), _ptr(v_cache), tokens, num_qo_heads,
