@@ -147,7 +147,6 @@ __device__ int request_by_size(const DecodeParams &p, int item, int &kv_len) {
     }
     return c;
   };
-  unsigned lo = 0, hi = 0;                      // class counts, 6 bits each (a group adds <= 32)
   int total[kClasses];
 #pragma unroll
   for (int k = 0; k < kClasses; ++k) total[k] = 0;
@@ -162,10 +161,9 @@ __device__ int request_by_size(const DecodeParams &p, int item, int &kv_len) {
 #pragma unroll
     for (int v = 0; v < kHeld; ++v)
       if (v == u) cls_of[v] = c;
-    lo = c >= 0 && c < kLow ? 1u << (6 * c) : 0u;
-    hi = c >= kLow ? 1u << (6 * (c - kLow)) : 0u;
-    lo = __reduce_add_sync(0xffffffffu, lo);
-    hi = __reduce_add_sync(0xffffffffu, hi);
+    // class counts of the group, 6 bits per class (a group adds at most 32)
+    const unsigned lo = __reduce_add_sync(0xffffffffu, c >= 0 && c < kLow ? 1u << (6 * c) : 0u);
+    const unsigned hi = __reduce_add_sync(0xffffffffu, c >= kLow ? 1u << (6 * (c - kLow)) : 0u);
 #pragma unroll
     for (int k = 0; k < kClasses; ++k)
       total[k] += static_cast<int>(((k < kLow ? lo : hi) >> (6 * (k < kLow ? k : k - kLow))) & 63u);

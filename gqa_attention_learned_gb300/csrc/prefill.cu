@@ -97,89 +97,61 @@ __device__ __forceinline__ void pack_chunk(uint32_t (&r)[32], uint64_t scale2, u
   }
 }
 
-// Block-wide exclusive prefix sum of one value per thread (kThreads
-// threads); `total` gets the sum.
-__device__ __forceinline__ int block_excl_scan(int v, int *scratch, int &total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) scratch[warp] = x;
-  __syncthreads();
-  int before = 0, tot = 0;
-#pragma unroll
-  for (int w = 0; w < kThreads / 32; ++w) {
-    const int sw = scratch[w];
-    before += w < warp ? sw : 0;
-    tot += sw;
-  }
-  __syncthreads();
-  total = tot;
-  return before + x - v;
-}
-
 // Request of dispatch slot `slot` with the requests heaviest first: 8 size
 // classes of ceil(kv_len / 16) pages (largest first), request order within a
-// class.  Every CTA derives the same order from kv_lens (a reduction and a
-// block scan), so the last wave holds the short requests.
+// class.  Every warp derives the same order from kv_lens on its own (no block
+// barrier; the class by one float multiply, the class counts of 32 requests
+// at a time by two warp reductions of packed 6-bit fields, the request by one
+// ballot), so the last wave holds the short requests.  Returns -1 past the
+// last request.
 __device__ int request_by_size(const PrefillParams &p, int slot) {
-  constexpr int kClasses = 8;
-  __shared__ int scratch[kThreads / 32], totals[kClasses], owner;
-  const int max_pages = max(1, cdiv(p.max_kv_len, kPageSize));
-  auto size_class = [&](int b) {
-    const int pages = cdiv(max(p.kv_lens[b], 0), kPageSize);
-    return min(kClasses - 1, static_cast<int>(static_cast<long long>(pages) * kClasses / (max_pages + 1)));
+  constexpr int kClasses = 8, kLow = 4;         // classes 0..3 in the first word, 4..7 in the second
+  constexpr int kHeld = 8;                      // groups of 32 classes kept in registers
+  const int lane = threadIdx.x & 31;
+  const int groups = cdiv(p.num_seqs, 32);
+  const float per_page =
+      static_cast<float>(kClasses) / static_cast<float>(max(1, cdiv(p.max_kv_len, kPageSize)) + 1);
+  auto class_of = [&](int b) {
+    if (b >= p.num_seqs) return -1;
+    const int pages = cdiv(max(__ldg(p.kv_lens + b), 0), kPageSize);
+    return min(kClasses - 1, __float2int_rz(static_cast<float>(pages) * per_page));
   };
-  const int per = cdiv(p.num_seqs, kThreads);
-  const int b0 = min(p.num_seqs, static_cast<int>(threadIdx.x) * per);
-  const int b1 = min(p.num_seqs, b0 + per);
-  int cnt[kClasses];
+  int held[kHeld];
+  int total[kClasses];
 #pragma unroll
-  for (int k = 0; k < kClasses; ++k) cnt[k] = 0;
-  for (int b = b0; b < b1; ++b) {
-    const int c = size_class(b);
+  for (int k = 0; k < kClasses; ++k) total[k] = 0;
+  for (int u = 0; u < groups; ++u) {
+    const int c = class_of(u * 32 + lane);
 #pragma unroll
-    for (int k = 0; k < kClasses; ++k) cnt[k] += c == k ? 1 : 0;
+    for (int v = 0; v < kHeld; ++v)
+      if (v == u) held[v] = c;
+    const unsigned lo = __reduce_add_sync(0xffffffffu, c >= 0 && c < kLow ? 1u << (6 * c) : 0u);
+    const unsigned hi = __reduce_add_sync(0xffffffffu, c >= kLow ? 1u << (6 * (c - kLow)) : 0u);
+#pragma unroll
+    for (int k = 0; k < kClasses; ++k)
+      total[k] += static_cast<int>(((k < kLow ? lo : hi) >> (6 * (k % kLow))) & 63u);
   }
-  if (threadIdx.x < kClasses) totals[threadIdx.x] = 0;
-  if (threadIdx.x == 0) owner = -1;
-  __syncthreads();
-#pragma unroll
-  for (int k = 0; k < kClasses; ++k)
-    if (cnt[k]) atomicAdd(&totals[k], cnt[k]);
-  __syncthreads();
   int rank = slot, cls = -1;
-  for (int k = kClasses - 1; k >= 0; --k) {          // uniform over the CTA
-    if (rank < totals[k]) {
-      cls = k;
-      break;
-    }
-    rank -= totals[k];
-  }
-  if (cls >= 0) {
-    int mine = 0;
 #pragma unroll
-    for (int k = 0; k < kClasses; ++k) mine += k == cls ? cnt[k] : 0;
-    int in_cls;
-    const int off = block_excl_scan(mine, scratch, in_cls);
-    if (rank >= off && rank < off + mine) {
-      int seen = off;
-      for (int b = b0; b < b1; ++b) {
-        if (size_class(b) == cls) {
-          if (seen == rank) {
-            owner = b;
-            break;
-          }
-          ++seen;
-        }
-      }
+  for (int k = kClasses - 1; k >= 0; --k) {
+    if (cls < 0) {
+      if (rank < total[k]) cls = k;
+      else rank -= total[k];
     }
   }
-  __syncthreads();
-  return owner;
+  if (cls < 0) return -1;
+  for (int u = 0; u < groups; ++u) {
+    int c = -1;
+#pragma unroll
+    for (int v = 0; v < kHeld; ++v)
+      if (v == u) c = held[v];
+    if (u >= kHeld) c = class_of(u * 32 + lane);
+    const unsigned hit = __ballot_sync(0xffffffffu, c == cls);
+    const int n = __popc(hit);
+    if (rank < n) return u * 32 + static_cast<int>(__fns(hit, 0, rank + 1));
+    rank -= n;
+  }
+  return -1;                                    // not reached: the classes cover every request
 }
 
 template <bool kPaged, bool kVerify>
