@@ -111,14 +111,17 @@ def _on(dev):
 
 
 _plans = {}
+_PLANS_KEPT = 4096
 
 
 def _plan(fn, *args):
     """fn(*args) for the current device, memoised: plans depend only on
-    host-side sizes and the device's SM count."""
+    host-side sizes and the device's SM count (at most _PLANS_KEPT kept)."""
     key = (fn.__name__, torch.cuda.current_device()) + args
     hit = _plans.get(key)
     if hit is None:
+        if len(_plans) >= _PLANS_KEPT:
+            _plans.clear()
         hit = _plans[key] = fn(*args)
     return hit
 
