@@ -24,8 +24,37 @@ def _gqa(rng):
     return GROUPS[int(rng.integers(len(GROUPS)))]
 
 
+class _launch_mode:
+    """Programmatic dependent launch on or off for the calls inside."""
+
+    def __init__(self, on):
+        self.on = on
+
+    def __enter__(self):
+        self.prev = sa.set_programmatic_launch(self.on)
+
+    def __exit__(self, *exc):
+        sa.set_programmatic_launch(self.prev)
+
+
+def _twice(call):
+    """Two calls back to back (the second may overlap the first when launched
+    programmatically); both results must agree bit for bit."""
+    a = call()
+    b = call()
+    torch.cuda.synchronize()
+    def bits(t):                        # NaN rows compare by their bits
+        return t.view(torch.int16) if t.dtype == torch.bfloat16 else t.view(torch.int32)
+
+    for x, y in zip(a, b):
+        if x is not None:
+            assert torch.equal(bits(x), bits(y))
+    return b
+
+
+@pytest.mark.parametrize("programmatic", [False, True])
 @pytest.mark.parametrize("case", range(12))
-def test_random_decode(case):
+def test_random_decode(case, programmatic):
     rng = np.random.default_rng(1000 + case)
     hq, hkv = _gqa(rng)
     batch = int(rng.integers(1, 24))
@@ -34,8 +63,9 @@ def test_random_decode(case):
                                min_len=0, max_len=max_len, special_sinks=bool(case % 2))
     splits = int(rng.choice([0, 1, 2, 5, 64]))
     args = [w[n].to(DEV) for n in ("q", "k_cache", "v_cache", "page_table", "kv_lens", "sinks")]
-    out, lse = sa.decode(*args, w["scale"], max(1, w["max_kv_len"]), num_splits=splits)
-    torch.cuda.synchronize()
+    with _launch_mode(programmatic):
+        out, lse = _twice(lambda: sa.decode(*args, w["scale"], max(1, w["max_kv_len"]),
+                                            num_splits=splits))
     ro, rl = oracle.decode(to_np(w["q"]), Bf16Pool(w["k_cache"]), Bf16Pool(w["v_cache"]),
                            w["page_table"].numpy(), w["kv_lens"].numpy(),
                            w["sinks"].numpy().astype(np.float64), w["scale"])
@@ -43,8 +73,9 @@ def test_random_decode(case):
     assert_lse_close(lse.cpu(), rl, f"lse case {case}")
 
 
+@pytest.mark.parametrize("programmatic", [False, True])
 @pytest.mark.parametrize("case", range(12))
-def test_random_verify(case):
+def test_random_verify(case, programmatic):
     rng = np.random.default_rng(3000 + case)
     hq, hkv = _gqa(rng)
     q_len = int(rng.integers(1, 20))
@@ -59,8 +90,9 @@ def test_random_verify(case):
     splits = 0 if big else int(rng.choice([0, 1, 3]))
     args = [w[n].to(DEV) for n in ("q", "k_cache", "v_cache", "page_table", "kv_lens", "sinks")]
     mask = None if w["tree_mask"] is None else w["tree_mask"].to(DEV)
-    out, lse = sa.verify(*args, w["scale"], w["max_kv_len"], tree_mask=mask, num_splits=splits)
-    torch.cuda.synchronize()
+    with _launch_mode(programmatic):
+        out, lse = _twice(lambda: sa.verify(*args, w["scale"], w["max_kv_len"], tree_mask=mask,
+                                            num_splits=splits))
     reqs = list(range(batch)) if batch <= 12 else sorted(set(rng.integers(0, batch, 10).tolist()))
     ro, rl = oracle.verify(to_np(w["q"][reqs]), Bf16Pool(w["k_cache"]), Bf16Pool(w["v_cache"]),
                            w["page_table"].numpy()[reqs], w["kv_lens"].numpy()[reqs],
