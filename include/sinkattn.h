@@ -37,7 +37,9 @@
  *     memory outside the given buffers is touched.
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *     default stream), never synchronises, allocates nothing, and keeps no
- *     state beyond a per-device cache of the SM count.  Calls are thread-safe.
+ *     state beyond per-device caches (the SM count, kernel attributes set
+ *     once) and the process-wide launch mode of
+ *     sinkattn_set_programmatic_launch.  Calls are thread-safe.
  *   - Return value: a sinkattn_status.  Argument checks happen on the host
  *     before any launch; SINKATTN_CUDA_ERROR reports a launch failure.
  */
