@@ -259,6 +259,13 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
     return j < n_my ? table[first + j * kNW] : -1;
   };
   int ids_cur = load_ids(0), ids_next = load_ids(32);
+  // This warp's first pages into L2 while the previous kernel on the stream
+  // may still be draining (a programmatic launch); the copies below then
+  // find them there.
+  if (lane < kStages && ids_cur >= 0 && ids_cur < p.num_pages) {
+    tma_prefetch_l2_3d(&kmap, 0, kvh * kPageSize, ids_cur);
+    tma_prefetch_l2_3d(&vmap, 0, kvh * kPageSize, ids_cur);
+  }
 
   // Up to here only kv_lens and page_table were read; everything below may
   // depend on the previous kernel on the stream (q, the caches, sinks, masks,

@@ -99,6 +99,15 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Brings the 3-D tile at (x, y, z) of `map` into L2 (no shared memory, no
+// completion to wait for).  L2 is coherent with every write to global
+// memory, so a prefetch never makes a later read stale.
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap *map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
+               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 // ------------------------------------------- programmatic dependent launch
 // Blocks until the kernel launched before this one on the stream has finished
 // and its writes are visible; returns at once for a launch without the
