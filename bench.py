@@ -45,7 +45,7 @@ DECODE_WORKLOAD = ("gpt-oss-20b decode: 64 q / 8 KV heads, head_dim 64, batch 64
 # DRAM bytes (read + write) of one headline decode launch from an ncu capture
 # (profiles/decode_gptoss20b_b64.md), valid only for the kernel sources it was
 # taken on: a change to them reports the traffic as unknown.
-DECODE_TRAFFIC = {"sources_sha256_16": "813ad0679a2995ea", "bytes": 265_554_176}
+DECODE_TRAFFIC = {"sources_sha256_16": "6a66e5fd8f22a6e4", "bytes": 265_716_480}
 DECODE_SOURCES = ("gqa_attention_learned_gb300/csrc/decode.cu",
                   "gqa_attention_learned_gb300/csrc/kernels.cuh",
                   "gqa_attention_learned_gb300/csrc/ptx.cuh")
