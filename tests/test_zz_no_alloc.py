@@ -62,3 +62,40 @@ def test_static_scratch_rejects_plans_beyond_its_size():
     with pytest.raises(sa.SinkAttnError) as e:
         sa.decode_static_scratch(q, kc, kc, table, lens, sinks, 0.125, 4096, num_splits=8)
     assert e.value.status == sa.WORKSPACE_TOO_SMALL
+
+
+def test_static_scratch_chained_under_programmatic_launch():
+    # decode_static_scratch calls back to back with programmatic launch on,
+    # each reading the previous call's output as its q: the scratch clear
+    # (a memset on the stream) and the previous decode both precede the
+    # kernel, which reads q only after its dependency wait
+    w = workloads.decode_batch(seed=19, batch=24, min_len=1500, max_len=6000)
+    args = _inputs(w)
+    max_kv = w["max_kv_len"]
+
+    def chain():
+        q, outs = args[0], []
+        for _ in range(4):
+            out, lse = sa.decode_static_scratch(q, *args[1:], w["scale"], max_kv)
+            outs.append((out, lse))
+            q = out
+        torch.cuda.synchronize()
+        return outs
+
+    prev = sa.set_programmatic_launch(True)
+    try:
+        fast = chain()
+    finally:
+        sa.set_programmatic_launch(False)
+    try:
+        q, slow = args[0], []
+        for _ in range(4):
+            out, lse = sa.decode(q, *args[1:], w["scale"], max_kv)
+            torch.cuda.synchronize()
+            slow.append((out, lse))
+            q = out
+    finally:
+        sa.set_programmatic_launch(prev)
+    for (a, la), (b, lb) in zip(fast, slow):
+        assert_out_close(a.cpu(), to_np(b), "chained static-scratch out")
+        assert_lse_close(la.cpu(), to_np(lb), "chained static-scratch lse")
