@@ -175,3 +175,31 @@ def test_tensor_core_route_large_batch():
     ro, rl = ref_verify(w, reqs)
     assert_out_close(out[reqs], ro)
     assert_lse_close(lse[reqs], rl)
+
+
+@pytest.mark.parametrize("programmatic", [False, True])
+def test_tensor_core_route_long_requests_back_to_back(programmatic):
+    """4 tokens x 8 heads = 32 rows per KV head on the tensor-core route with
+    long requests (up to 32 key tiles) and many launches back to back, in
+    both launch modes: every output finite (no wait gave up), sampled
+    requests equal the oracle, every launch equal to the first."""
+    w = workloads.verify_batch(seed=71, batch=64, q_len=4, min_len=2000, max_len=4096)
+    assert sa.verify_plan(64, 4, 64, 8, w["max_kv_len"]) == (1, 0)
+    q, kc, vc, table, lens, sinks = [w[n].to(DEV) for n in
+                                     ("q", "k_cache", "v_cache", "page_table", "kv_lens", "sinks")]
+    prev = sa.set_programmatic_launch(programmatic)
+    try:
+        outs = [sa.verify(q, kc, vc, table, lens, sinks, w["scale"], w["max_kv_len"])
+                for _ in range(12)]
+        torch.cuda.synchronize()
+    finally:
+        sa.set_programmatic_launch(prev)
+    first_out, first_lse = outs[0]
+    assert torch.isfinite(first_out.float()).all() and torch.isfinite(first_lse).all()
+    for out, lse in outs[1:]:
+        assert torch.equal(out.view(torch.int16), first_out.view(torch.int16))
+        assert torch.equal(lse.view(torch.int32), first_lse.view(torch.int32))
+    reqs = [0, 17, 40, 63]
+    ro, rl = ref_verify(w, reqs)
+    assert_out_close(first_out.cpu()[reqs], ro)
+    assert_lse_close(first_lse.cpu()[reqs], rl)
