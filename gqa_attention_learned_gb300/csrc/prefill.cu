@@ -33,6 +33,17 @@
 // V rows past a request's last key are zeroed in shared memory before the PV
 // MMA (0 * NaN would poison whole rows); score columns past a row's causal
 // limit are masked by index.
+//
+// Verification (kVerify; "Accelerating Sonar through speculation", sections
+// "Target-Draft", "MTP" and "EAGLE"): the query rows of one KV head of one
+// request -- its q_len newest tokens x the group's heads, ordered (token,
+// head) -- form the 128-row tile (Q by one 3-D box {64, group, 128/group}).
+// Each softmax thread takes its row's token for the causal limit (or its
+// tree bits for the draft keys) and its head for the sink; warps without
+// rows stay out of the barrier counts.  Requests go heaviest first (ranked
+// from kv_lens by every warp), and under a programmatic launch the ranking,
+// the page-table reads and the shared / tensor memory set-up run before the
+// wait for the previous kernel on the stream.
 
 #include "kernels.cuh"
 #include "ptx.cuh"
