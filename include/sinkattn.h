@@ -137,6 +137,9 @@ SINKATTN_API int sinkattn_decode_plan(int batch, int num_qo_heads, int num_kv_he
  * Long contexts run as num_splits KV chunks per (request, KV head), the sink
  * entering chunk 0 only; the last chunk to finish merges them by
  * log-sum-exp inside the same kernel.
+ * Limits: batch <= 65535, and num_kv_heads times the 8-row query blocks per
+ * KV head (ceil(group / 8) for decode) <= 65535; larger calls return
+ * SINKATTN_UNSUPPORTED without launching.
  */
 SINKATTN_API int sinkattn_decode(const void *q, const void *k_cache, const void *v_cache,
                     const int32_t *page_table, int max_pages_per_seq,
