@@ -99,6 +99,19 @@ def test_decode_rejects_on_host(lib):
     assert _raw_decode(lib, q=odd, k=fake, v=fake, table=fake, lens=fake, sinks=fake,
                        out=fake) == sa.INVALID_ARGUMENT                  # misaligned q
     assert _raw_decode(lib, batch=0) == sa.OK                            # nothing to do
+    ok = dict(q=fake, k=fake, v=fake, table=fake, lens=fake, sinks=fake, out=fake)
+    assert _raw_decode(lib, batch=65536, **ok) == sa.UNSUPPORTED          # documented limit
+    assert _raw_decode(lib, batch=1, hq=65536 * 8, hkv=65536, **ok) == sa.UNSUPPORTED
+
+
+def test_programmatic_launch_switch_is_host_state(lib):
+    prev = sa.set_programmatic_launch(True)
+    try:
+        assert lib.sinkattn_set_programmatic_launch(0) == 1
+        assert lib.sinkattn_set_programmatic_launch(5) == 0              # any non-zero = on
+        assert sa.set_programmatic_launch(False) is True
+    finally:
+        sa.set_programmatic_launch(prev)
 
 
 def test_prefill_rejects_on_host(lib):
