@@ -133,7 +133,8 @@ def _tc_batch(q_len, hq, hkv):
 @pytest.mark.parametrize("q_len,hq,hkv,tree", [(4, 64, 8, False), (8, 64, 8, True),
                                                (16, 64, 8, True), (32, 64, 8, True),
                                                (6, 32, 8, False), (2, 32, 2, True),
-                                               (32, 8, 8, True), (2, 128, 1, False)])
+                                               (32, 8, 8, True), (2, 128, 1, False),
+                                               (64, 64, 8, True)])
 def test_tensor_core_route(q_len, hq, hkv, tree):
     b = _tc_batch(q_len, hq, hkv)
     w = workloads.verify_batch(seed=300 + q_len + hq, batch=b, q_len=q_len, num_qo_heads=hq,
