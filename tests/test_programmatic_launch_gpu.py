@@ -264,3 +264,49 @@ def test_verify_chain_through_q(q_len, tree):
                            tree_mask=None if m is None else m.numpy())
     assert_out_close(fast[0].cpu(), ro)
     assert_lse_close(fast_lse[0].cpu(), rl)
+
+
+def test_tensor_core_verify_chain_with_invalid_requests():
+    """Tensor-core verification chained through q under programmatic launch,
+    with requests that have fewer keys than new tokens: their CTAs write NaN
+    rows after the dependency wait and leave without running the tile loop;
+    the other requests must equal the calls made one at a time."""
+    q_len = 4
+    w = workloads.verify_batch(seed=61, batch=64, q_len=q_len, max_len=900)
+    lens = w["kv_lens"].clone()
+    lens[5] = q_len - 1
+    lens[40] = 0
+    w["kv_lens"] = lens
+    d = _dev(w)
+    assert sa.verify_plan(64, q_len, 64, 8, w["max_kv_len"]) == (1, 0)
+
+    def run(sync_each):
+        q, outs = d["q"], []
+        for _ in range(4):
+            out = torch.full_like(q, float("nan"))
+            lse = torch.full(q.shape[:3], float("nan"), dtype=torch.float32, device=DEV)
+            sa.verify(q, d["k_cache"], d["v_cache"], d["page_table"], d["kv_lens"], d["sinks"],
+                      d["scale"], d["max_kv_len"], out=out, lse=lse)
+            if sync_each:
+                torch.cuda.synchronize()
+            outs.append((out, lse))
+            q = out
+        torch.cuda.synchronize()
+        return outs
+
+    with programmatic(True):
+        fast = run(False)
+    with programmatic(False):
+        slow = run(True)
+    for (a, la), (b, lb) in zip(fast, slow):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+        assert torch.equal(la.view(torch.int32), lb.view(torch.int32))
+    out0, lse0 = fast[0]
+    for bad in (5, 40):
+        assert torch.isnan(out0[bad].float()).all() and torch.isnan(lse0[bad]).all()
+    reqs = [0, 6, 39, 63]
+    ro, rl = oracle.verify(to_np(w["q"][reqs]), Bf16Pool(w["k_cache"]), Bf16Pool(w["v_cache"]),
+                           w["page_table"].numpy()[reqs], w["kv_lens"].numpy()[reqs],
+                           w["sinks"].numpy().astype(np.float64), w["scale"])
+    assert_out_close(out0.cpu()[reqs], ro)
+    assert_lse_close(lse0.cpu()[reqs], rl)
