@@ -42,25 +42,37 @@ DECODE_WORKLOAD = ("gpt-oss-20b decode: 64 q / 8 KV heads, head_dim 64, batch 64
 
 # ----------------------------------------------------------------- helpers
 
-# DRAM bytes (read + write) of one headline decode launch from an ncu capture
-# (profiles/decode_gptoss20b_b64.md), valid only for the kernel sources it was
-# taken on: a change to them reports the traffic as unknown.
-DECODE_TRAFFIC = {"sources_sha256_16": "6a66e5fd8f22a6e4", "bytes": 265_716_480}
-DECODE_SOURCES = ("gqa_attention_learned_gb300/csrc/decode.cu",
-                  "gqa_attention_learned_gb300/csrc/kernels.cuh",
-                  "gqa_attention_learned_gb300/csrc/ptx.cuh")
+# DRAM bytes (read + write) per launch of a kernel from one ncu capture of
+# the same workload, each valid only for the kernel sources it was taken on:
+# once a source changes, the traffic is reported as unknown (null).
+TRAFFIC = {
+    "decode": {"sources": ("gqa_attention_learned_gb300/csrc/decode.cu",
+                           "gqa_attention_learned_gb300/csrc/kernels.cuh",
+                           "gqa_attention_learned_gb300/csrc/ptx.cuh"),
+               "sha256_16": None, "bytes": None},
+    "prefill": {"sources": ("gqa_attention_learned_gb300/csrc/prefill.cu",
+                            "gqa_attention_learned_gb300/csrc/kernels.cuh",
+                            "gqa_attention_learned_gb300/csrc/ptx.cuh"),
+                "sha256_16": None, "bytes": None},
+}
 
 
-def decode_traffic():
+def sources_hash(files):
     import hashlib
     h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def kernel_traffic(kernel):
+    t = TRAFFIC[kernel]
     try:
-        for f in DECODE_SOURCES:
-            with open(os.path.join(ROOT, f), "rb") as fh:
-                h.update(fh.read())
+        ok = t["sha256_16"] is not None and sources_hash(t["sources"]) == t["sha256_16"]
     except OSError:
         return None
-    return DECODE_TRAFFIC["bytes"] if h.hexdigest()[:16] == DECODE_TRAFFIC["sources_sha256_16"] else None
+    return t["bytes"] if ok else None
 
 
 def load_peaks():
@@ -260,15 +272,20 @@ def run_decode_arm(args, rank, dev):
     ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step(i):
+    def step(i, mode=None):
         kc, vc = pools[i & 1]
         sa.decode(q, kc, vc, table, kv_lens, sinks, w["scale"], max_kv, out=out, lse=lse,
-                  num_splits=args.splits, workspace=ws, stream=stream)
+                  num_splits=args.splits, workspace=ws, stream=stream, programmatic=mode)
 
     with ClockSampler(index=torch.cuda.current_device()) as clocks:
         secs = _time_steps(torch, step, args.steps, args.warmup, stream)
     units, t_max, gbps = aggregate(nbytes * args.steps, secs, dev)
     launches_per_step = 1
+    # the same steps with every launch plain: each kernel starts only after
+    # the previous one has finished (no overlap of neighbouring launches)
+    plain_steps = max(args.steps, 100)
+    plain_secs = _time_steps(torch, lambda i: step(i, False), plain_steps, args.warmup, stream)
+    _, _, plain_gbps = aggregate(nbytes * plain_steps, plain_secs, dev)
 
     # end to end through the public call: each step's inputs (q, page table,
     # kv_lens) go host -> device in one copy of a packed pinned buffer, the
@@ -402,7 +419,9 @@ def run_decode_arm(args, rank, dev):
     kv_secs = _time_steps(torch, e2e_kv_step, kv_steps, 2, stream)
     _, _, kv_gbps = aggregate(nbytes * kv_steps, kv_secs, dev)
 
+    pool_mb = pools[0][0].numel() * pools[0][0].element_size() * 2 / 1e6
     return dict(w=w, nbytes=nbytes, secs=t_max, gbps=gbps / 1e9, splits=splits,
+                plain_gbps=plain_gbps / 1e9, plain_steps=plain_steps, pool_mb=pool_mb,
                 launches_per_step=launches_per_step, clocks=clocks.summary(),
                 e2e=dict(value=e2e_gbps / 1e9, unit="GB/s", h2d_bytes_per_step=h2d,
                          d2h_bytes_per_step=d2h, steps=e2e_steps,
@@ -565,6 +584,7 @@ def run_verify(args, rank, dev, peaks):
         secs = _time_steps(torch, step, steps, args.warmup, stream)
         _, t, bps = aggregate(nbytes * steps, secs, dev)
         res[label] = dict(q_len=q_len, tree=tree, splits=splits, bytes_per_step=nbytes,
+                          kernel=verify_kernel(len(lens), q_len, hq, hkv, w["max_kv_len"]),
                           ms_per_step=1e3 * t / steps, value=round(bps / 1e9, 2), unit="GB/s",
                           frac_of_hbm=round(bps / 1e9 / peaks["hbm_gbs"], 4))
         del pools, q
@@ -572,7 +592,22 @@ def run_verify(args, rank, dev, peaks):
     return dict(workload="draft-token verification on the gpt-oss-20b decode batch: 64 requests, "
                          "kv_len U[q_len,4096], 64 q / 8 KV heads, bf16 paged KV; two KV pool "
                          "copies alternate (inputs larger than L2)",
-                kernel="decode_kernel<2, true> (rows = tokens x heads of a KV head)", runs=res)
+                runs=res)
+
+
+def verify_kernel(batch, q_len, hq, hkv, max_kv_len, num_sms=152):
+    """Which kernel sinkattn_verify runs for these sizes with num_splits = 0
+    (the library's rule, stated in include/sinkattn.h): the tensor-core
+    kernel for >= 24 query rows per KV head, a group dividing 128, at most
+    8192 keys and a wave of (request, KV head) tiles; else the mma.sync
+    decode kernel with 8 or 16 rows per CTA."""
+    g = hq // hkv
+    tiles = -(-q_len // max(1, 128 // g)) if 128 % g == 0 else 0
+    if (q_len >= 2 and 128 % g == 0 and q_len * g >= 24 and -(-max_kv_len // 16) <= 512
+            and tiles * batch * hkv >= 2 * num_sms):
+        return "prefill_kernel<true, true> (tcgen05; rows = tokens x heads of a KV head)"
+    nb = 2 if q_len * g > 8 else 1
+    return f"decode_kernel<{nb}, true> (mma.sync; rows = tokens x heads of a KV head)"
 
 
 def run_prologue(args, rank, dev, peaks):
@@ -667,7 +702,8 @@ def run_prefill(args, rank, dev, peaks):
                           "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                           "frac": round(tf / peaks["bf16_tflops"], 4),
                           "frac_of_sustained": round(tf / peaks["bf16_tflops_sustained"], 4),
-                          "traffic": None, "kernel": "prefill_kernel<false>"})
+                          "traffic": kernel_traffic("prefill"),
+                          "kernel": "prefill_kernel<false, false>"})
 
 
 def run_mixed(args, rank, dev, peaks):
@@ -735,6 +771,47 @@ def run_mixed(args, rank, dev, peaks):
                 combined_roofline_frac=round(ideal / (t_all / steps), 4))
 
 
+def section_summary(extra, peaks):
+    """Flat numeric figures of the extra sections (GB/s, TFLOP/s and
+    fractions of the measured peaks) for the printed line; the full sections
+    go to --details."""
+    hbm, tf = peaks["hbm_gbs"], peaks["bf16_tflops"]
+    out = {}
+    if "long_decode" in extra:
+        r = extra["long_decode"]["runs"]["auto"]
+        out.update(long_decode_gbps=round(r["value"], 1), long_decode_frac=round(r["value"] / hbm, 4),
+                   long_decode_splits=r["splits"])
+        r8 = extra["long_decode"]["runs"]["8 splits"]
+        out.update(long_decode_8split_frac=round(r8["value"] / hbm, 4))
+    if "graph_decode" in extra:
+        g = extra["graph_decode"]
+        out.update(graph_decode_frac=g["frac_of_hbm"],
+                   graph10_decode_frac=g["ten_step_graph"]["frac_of_hbm"])
+    if "verify" in extra:
+        for key, label in (("verify_mtp2", "mtp 2 tokens"), ("verify_4tok", "4 tokens causal"),
+                           ("verify_tree8", "8-node tree")):
+            r = extra["verify"]["runs"].get(label)
+            if r:
+                out[key + "_gbps"] = r["value"]
+                out[key + "_frac"] = r["frac_of_hbm"]
+    if "prefill" in extra:
+        p = extra["prefill"]["roofline"]
+        out.update(prefill_tflops=p["achieved"], prefill_frac=p["frac"],
+                   prefill_frac_sustained=p["frac_of_sustained"], prefill_traffic=p["traffic"])
+    if "mixed" in extra:
+        m = extra["mixed"]
+        out.update(mixed_decode_gbps=m["decode"]["value"],
+                   mixed_decode_frac=round(m["decode"]["value"] / hbm, 4),
+                   mixed_extend_tflops=m["extend"]["value"],
+                   mixed_extend_frac=round(m["extend"]["value"] / tf, 4),
+                   mixed_combined_frac=m["combined_roofline_frac"])
+    if "prologue" in extra:
+        r = extra["prologue"]["runs"].get("prefill 4 sequences")
+        if r:
+            out.update(prologue_prefill_frac=r["frac_of_hbm"])
+    return out
+
+
 def gpu_arm(args):
     import torch
 
@@ -765,6 +842,14 @@ def gpu_arm(args):
             extra["prefill"] = run_prefill(args, rank, dev, peaks)
         if "mixed" in sections:
             extra["mixed"] = run_mixed(args, rank, dev, peaks)
+    roofline = {"bound": "hbm", "achieved": round(kernel_gbps, 2), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(kernel_gbps / peaks["hbm_gbs"], 4),
+                "traffic": kernel_traffic("decode"), "peak_source": peak_src,
+                "kernel": "decode_kernel<1, false>",
+                "bytes_per_launch": d["nbytes"],
+                "plain_launch_gbps": round(d["plain_gbps"], 1),
+                "plain_launch_frac": round(d["plain_gbps"] / peaks["hbm_gbs"], 4)}
+    roofline.update(section_summary(extra, peaks))
     line = {
         "metric": METRIC, "value": round(d["gbps"], 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
@@ -774,25 +859,22 @@ def gpu_arm(args):
                    "num_kv_heads": 8, "head_dim": 64, "page_size": 16,
                    "kv_tokens": sum(int(x) for x in d["w"]["kv_lens"]),
                    "num_splits": d["splits"],
-                   "launch": "plain" if args.plain_launch else
-                             "programmatic dependent launch (a decode ranks its requests and "
-                             "reads its first page ids while the previous kernel drains)",
-                   "l2": "inputs larger than L2: two KV pool copies (2 x 671 MB) alternate"},
-        "pct_of_hbm_peak": round(100 * d["gbps"] / peaks["hbm_gbs"], 2),
-        "roofline": {"bound": "hbm", "achieved": round(kernel_gbps, 2),
-                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(kernel_gbps / peaks["hbm_gbs"], 4),
-                     "traffic": decode_traffic(), "peak_source": peak_src,
-                     "kernel": "decode_kernel<1, false> (whole requests, heaviest first; "
-                               "split plans merge their chunks inside the kernel)",
-                     "bytes_per_launch": d["nbytes"]},
-        "e2e": d["e2e"], "e2e_kv_h2d": d["e2e_kv_h2d"],
+                   "launch": "plain" if args.plain_launch else "programmatic dependent launch",
+                   "l2": f"inputs larger than L2: two KV pool copies "
+                         f"(2 x {d['pool_mb']:.0f} MB) alternate"},
+        "roofline": roofline,
+        "e2e": {k: v for k, v in d["e2e"].items() if k != "note"},
         "gpu_launches": args.steps * d["launches_per_step"],
         "clocks": d["clocks"],
-        "extra": extra,
     }
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
+    if rank == 0 and args.details:
+        with open(args.details, "w") as f:
+            json.dump(dict(line=line, e2e=d["e2e"], e2e_kv_h2d=d["e2e_kv_h2d"],
+                           plain_launch=dict(steps=d["plain_steps"],
+                                             value=round(d["plain_gbps"], 2)),
+                           extra=extra), f, indent=1)
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -918,6 +1000,8 @@ def main():
                     help="launch decode kernels without programmatic dependent launch")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--details", default=None,
+                    help="write the full sections (e2e variants, per-run figures) to this JSON file")
     ap.add_argument("--oracle-worker", default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.oracle_worker is not None:

@@ -27,14 +27,21 @@ SIGNATURES = {
     "sinkattn_set_programmatic_launch": (_c_int, [_c_int]),
     "sinkattn_decode_plan": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                       ctypes.POINTER(_c_int), ctypes.POINTER(_c_size)]),
+    "sinkattn_decode_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
     "sinkattn_decode": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _vp, _c_float, _vp, _vp,
                                  _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                  _vp, _c_size, _vp]),
+    "sinkattn_decode_ex": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _vp, _c_float, _vp, _vp,
+                                    _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                    _c_int, _vp, _c_size, _c_int, _vp]),
     "sinkattn_verify_plan": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                       _c_int, ctypes.POINTER(_c_int), ctypes.POINTER(_c_size)]),
     "sinkattn_verify": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _vp, _vp, _c_float, _vp, _vp,
                                  _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                  _c_int, _vp, _c_size, _vp]),
+    "sinkattn_verify_ex": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _vp, _vp, _c_float, _vp,
+                                    _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                    _c_int, _c_int, _vp, _c_size, _c_int, _vp]),
     "sinkattn_prefill": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _vp, _c_float, _vp,
                                   _vp, _c_int, _c_int, _c_int, _vp]),
     "sinkattn_prefill_paged": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _vp, _c_int,
@@ -52,6 +59,7 @@ SIGNATURES = {
 }
 
 STATIC_SCRATCH_BYTES = 16 << 20
+LAUNCH_DEFAULT, LAUNCH_PLAIN, LAUNCH_PROGRAMMATIC = 0, 1, 2
 ROPE_HALF, ROPE_INTERLEAVED = 0, 1
 MAX_VERIFY_TOKENS = 64
 
@@ -87,11 +95,19 @@ def status_string(status):
 
 
 def set_programmatic_launch(enable):
-    """Process-wide switch for programmatic dependent launch of the decode
-    and verification kernels (decode, decode_static_scratch, verify); returns
-    the previous setting.  While on, kv_lens and page_table of a call must not be
-    written by the kernel launched just before it on the stream."""
+    """Process-wide DEFAULT launch mode of the decode and verification
+    kernels (decode, decode_static_scratch, verify called without
+    `programmatic=`); returns the previous setting.  In programmatic mode,
+    kv_lens and page_table of a call must not be written by the kernel
+    launched just before it on the stream."""
     return bool(load().sinkattn_set_programmatic_launch(1 if enable else 0))
+
+
+def _launch_flags(programmatic):
+    """None: the process-wide default; True / False: this call's own mode."""
+    if programmatic is None:
+        return LAUNCH_DEFAULT
+    return LAUNCH_PROGRAMMATIC if programmatic else LAUNCH_PLAIN
 
 
 def _check(fn, status):
@@ -162,11 +178,18 @@ def decode_plan(batch, num_qo_heads, num_kv_heads, max_kv_len, num_splits=0, num
     return s.value, w.value
 
 
+def decode_workspace_bytes(batch, num_qo_heads, num_splits, head_dim=64):
+    """Upper bound on decode's workspace for an explicit split count, valid
+    for any KV head count (host only; 0 for one split)."""
+    return int(load().sinkattn_decode_workspace_bytes(batch, num_qo_heads, head_dim, num_splits))
+
+
 def decode(q, k_cache, v_cache, page_table, kv_lens, sinks, scale, max_kv_len, *, out=None,
-           lse=None, num_splits=0, workspace=None, stream=None, want_lse=True):
+           lse=None, num_splits=0, workspace=None, stream=None, want_lse=True, programmatic=None):
     """Paged decode.  q [B, Hq, 64] bf16; caches [pages, Hkv, 16, 64] bf16;
     page_table [B, max_pages] int32; kv_lens [B] int32; sinks [Hq] fp32.
-    Returns (out [B, Hq, 64] bf16, lse [B, Hq] fp32 or None)."""
+    programmatic: None = the process-wide default launch mode, True / False =
+    this call's own.  Returns (out [B, Hq, 64] bf16, lse [B, Hq] fp32 or None)."""
     dev = q.device
     _want(q, "q", torch.bfloat16, 3)
     _want(k_cache, "k_cache", torch.bfloat16, 4, dev)
@@ -189,11 +212,11 @@ def decode(q, k_cache, v_cache, page_table, kv_lens, sinks, scale, max_kv_len, *
             # zero-filled once; decode leaves it ready for the next call
             workspace = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
         ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
-        _check("sinkattn_decode", load().sinkattn_decode(
+        _check("sinkattn_decode_ex", load().sinkattn_decode_ex(
             _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table), page_table.shape[1],
             _ptr(kv_lens), _ptr(sinks), float(scale), _ptr(out), _ptr(lse), batch, hq, hkv, d,
             page, num_pages, int(max_kv_len), int(num_splits), _ptr(workspace), ws_len,
-            _stream(stream)))
+            _launch_flags(programmatic), _stream(stream)))
     return out, lse
 
 
@@ -210,12 +233,14 @@ def verify_plan(batch, q_len, num_qo_heads, num_kv_heads, max_kv_len, num_splits
 
 
 def verify(q, k_cache, v_cache, page_table, kv_lens, sinks, scale, max_kv_len, *, tree_mask=None,
-           out=None, lse=None, num_splits=0, workspace=None, stream=None, want_lse=True):
+           out=None, lse=None, num_splits=0, workspace=None, stream=None, want_lse=True,
+           programmatic=None):
     """Verification of the q_len newest tokens of every request (speculative
     decoding).  q [B, q_len, Hq, 64] bf16; the tokens are the last q_len keys
     of each request's paged KV.  tree_mask: None (causal) or int64
     [B, q_len] holding the uint64 bit masks (bit u of row i: token i sees
-    draft token u).  Returns (out [B, q_len, Hq, 64], lse [B, q_len, Hq])."""
+    draft token u).  programmatic: as for decode.  Returns
+    (out [B, q_len, Hq, 64], lse [B, q_len, Hq])."""
     dev = q.device
     _want(q, "q", torch.bfloat16, 4)
     _want(k_cache, "k_cache", torch.bfloat16, 4, dev)
@@ -239,11 +264,11 @@ def verify(q, k_cache, v_cache, page_table, kv_lens, sinks, scale, max_kv_len, *
         if workspace is None and ws_bytes:
             workspace = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
         ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
-        _check("sinkattn_verify", load().sinkattn_verify(
+        _check("sinkattn_verify_ex", load().sinkattn_verify_ex(
             _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table), page_table.shape[1],
             _ptr(kv_lens), _ptr(tree_mask), _ptr(sinks), float(scale), _ptr(out), _ptr(lse), batch,
             q_len, hq, hkv, d, page, num_pages, int(max_kv_len), int(num_splits), _ptr(workspace),
-            ws_len, _stream(stream)))
+            ws_len, _launch_flags(programmatic), _stream(stream)))
     return out, lse
 
 

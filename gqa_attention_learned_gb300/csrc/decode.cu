@@ -602,14 +602,14 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
 
 template <int NB, bool kVerify>
 cudaError_t launch_variant(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParams &p,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, bool programmatic) {
   cudaError_t err = set_smem_once<decode_kernel<NB, kVerify>>(kSmemBytes);
   if (err != cudaSuccess) return err;
   const unsigned long long ctas =
       static_cast<unsigned long long>(p.num_splits) * p.batch * p.num_kv_heads * p.head_blocks;
   if (ctas > 0x7fffffffull) return cudaErrorInvalidConfiguration;
   return launch_kernel(decode_kernel<NB, kVerify>, static_cast<unsigned>(ctas), kNW * 32,
-                       kSmemBytes, stream, programmatic_launch(), kmap, vmap, p);
+                       kSmemBytes, stream, programmatic, kmap, vmap, p);
 }
 
 }  // namespace
@@ -622,12 +622,12 @@ int decode_ctas_per_sm() {
 int decode_max_splits() { return 1024; }
 
 cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParams &p,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, bool programmatic) {
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
   const bool verify = p.q_len > 1 || p.tree_mask != nullptr;
-  if (!verify && p.col_blocks == 1) return launch_variant<1, false>(kmap, vmap, p, stream);
-  if (p.col_blocks == 1) return launch_variant<1, true>(kmap, vmap, p, stream);
-  return launch_variant<2, true>(kmap, vmap, p, stream);
+  if (!verify && p.col_blocks == 1) return launch_variant<1, false>(kmap, vmap, p, stream, programmatic);
+  if (p.col_blocks == 1) return launch_variant<1, true>(kmap, vmap, p, stream, programmatic);
+  return launch_variant<2, true>(kmap, vmap, p, stream, programmatic);
 }
 
 }  // namespace sa

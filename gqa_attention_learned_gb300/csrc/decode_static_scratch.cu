@@ -1,7 +1,7 @@
 // sinkattn_decode_static_scratch: decode whose split scratch is a fixed
 // device array inside the library, for callers that cannot allocate device
-// memory.  It clears the array's merge counters and forwards to
-// sinkattn_decode with that array as the workspace.
+// memory.  It hands that array to the shared decode entry as the workspace,
+// asking it to clear the merge counters once every check has passed.
 
 #include "sinkattn.h"
 #include "kernels.cuh"
@@ -47,25 +47,18 @@ extern "C" SINKATTN_API int sinkattn_decode_static_scratch(
     int max_pages_per_seq, const int32_t *kv_lens, const float *sinks, float scale, void *out,
     float *lse, int batch, int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
     int num_pages, int max_kv_len, int num_splits, void *stream) {
-  if (batch == 0) return SINKATTN_OK;
-  int splits = num_splits;
-  size_t need = 0;
-  int st = sinkattn_decode_plan(batch, num_qo_heads, num_kv_heads, head_dim, page_size, max_kv_len,
-                                0, &splits, &need);
-  if (st != SINKATTN_OK) return st;
-  if (need > SINKATTN_STATIC_SCRATCH_BYTES) return SINKATTN_WORKSPACE_TOO_SMALL;
   void *scratch = nullptr;
-  st = scratch_for_current_device(&scratch);
-  if (st != SINKATTN_OK) return st;
-  // the merge counters must start at zero (a memset, not an allocation)
-  const size_t zero_bytes = sa::decode_counter_bytes(batch, num_qo_heads, num_kv_heads);
-  if (zero_bytes &&
-      cudaMemsetAsync(scratch, 0, zero_bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
-    cudaGetLastError();
-    return SINKATTN_CUDA_ERROR;
+  if (batch > 0) {
+    const int st = scratch_for_current_device(&scratch);
+    if (st != SINKATTN_OK) return st;
   }
-  return sinkattn_decode(q, k_cache, v_cache, page_table, max_pages_per_seq, kv_lens, sinks, scale,
-                         out, lse, batch, num_qo_heads, num_kv_heads, head_dim, page_size,
-                         num_pages, max_kv_len, num_splits, scratch, SINKATTN_STATIC_SCRATCH_BYTES,
-                         stream);
+  // decode_entry runs every argument check and the plan first; only a plan
+  // with more than one split then clears its merge counters (the first bytes
+  // of the array, within the plan's workspace size, which the size check
+  // keeps within the array) before the launch.  A refused call queues
+  // nothing, and a single-split call touches nothing in the array.
+  return sa::decode_entry(q, k_cache, v_cache, page_table, max_pages_per_seq, kv_lens, nullptr,
+                         sinks, scale, out, lse, batch, 1, num_qo_heads, num_kv_heads, head_dim,
+                         page_size, num_pages, max_kv_len, num_splits, scratch,
+                         SINKATTN_STATIC_SCRATCH_BYTES, SINKATTN_LAUNCH_DEFAULT, true, stream);
 }

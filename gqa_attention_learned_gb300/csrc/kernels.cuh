@@ -28,10 +28,6 @@ inline cudaError_t set_smem_once(int bytes) {
   if (err == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
   return err;
 }
-// Process-wide switch: decode and verification kernels launched with the
-// programmatic-serialization attribute (see sinkattn_set_programmatic_launch).
-bool programmatic_launch();
-
 // Launches `kernel` on `stream`; with `programmatic` the launch may start while
 // the previous kernel on the stream is still running (the kernel orders its
 // dependent reads and writes after grid_dependency_wait).
@@ -92,8 +88,11 @@ int decode_max_splits();
 // Bytes at the start of the decode workspace that must be zero before a call.
 size_t decode_counter_bytes(int batch, int num_qo_heads, int num_kv_heads, int q_len = 1);
 
+// `programmatic`: launch with the programmatic-serialization attribute (the
+// kernel waits for the previous kernel on the stream before touching anything
+// but kv_lens and the page table).
 cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap,
-                          const DecodeParams &p, cudaStream_t stream);
+                          const DecodeParams &p, cudaStream_t stream, bool programmatic);
 
 // ---------------------------------------------------------------- prefill
 struct PrefillParams {
@@ -118,9 +117,11 @@ struct PrefillParams {
   const uint64_t *tree_mask;
 };
 
+// `programmatic` applies to verification launches only; prefill and extend
+// always launch plainly.
 cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap,
                            const CUtensorMap &vmap, const PrefillParams &p,
-                           cudaStream_t stream);
+                           cudaStream_t stream, bool programmatic);
 
 // --------------------------------------------------------------- prologue
 struct PrologueParams {
@@ -137,5 +138,20 @@ struct PrologueParams {
 };
 
 cudaError_t launch_prologue(const PrologueParams &p, cudaStream_t stream);
+
+// ------------------------------------------------------------ C ABI layer
+// Decode / verification of q_len tokens per request, shared by
+// sinkattn_decode[_ex], sinkattn_verify[_ex] and
+// sinkattn_decode_static_scratch: every argument check, the split plan, then
+// the launch.  launch_flags is one of SINKATTN_LAUNCH_*.  With zero_counters,
+// a plan of more than one split first clears the workspace's merge counters
+// on the stream (cudaMemsetAsync, queued only after every check has passed);
+// a single-split plan touches no workspace at all.
+int decode_entry(const void *q, const void *k_cache, const void *v_cache,
+                 const int32_t *page_table, int max_pages_per_seq, const int32_t *kv_lens,
+                 const uint64_t *tree_mask, const float *sinks, float scale, void *out, float *lse,
+                 int batch, int q_len, int num_qo_heads, int num_kv_heads, int head_dim,
+                 int page_size, int num_pages, int max_kv_len, int num_splits, void *workspace,
+                 size_t workspace_bytes, int launch_flags, bool zero_counters, void *stream);
 
 }  // namespace sa

@@ -620,24 +620,25 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
 template <bool kPaged, bool kVerify>
 static cudaError_t launch_prefill_variant(const CUtensorMap &qmap, const CUtensorMap &kmap,
                            const CUtensorMap &vmap, const PrefillParams &p, unsigned ctas,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, bool programmatic) {
   cudaError_t err = set_smem_once<prefill_kernel<kPaged, kVerify>>(kSmemBytes);
   if (err != cudaSuccess) return err;
-  // verification follows the decode kernel's launch mode; prefill launches plainly
+  // verification follows the caller's launch mode; prefill launches plainly
   return launch_kernel(prefill_kernel<kPaged, kVerify>, ctas, kThreads, kSmemBytes, stream,
-                       kVerify && programmatic_launch(), qmap, kmap, vmap, p);
+                       kVerify && programmatic, qmap, kmap, vmap, p);
 }
 
 cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap,
-                           const CUtensorMap &vmap, const PrefillParams &p, cudaStream_t stream) {
+                           const CUtensorMap &vmap, const PrefillParams &p, cudaStream_t stream,
+                           bool programmatic) {
   static_assert(kSmemBytes <= 113 * 1024, "two CTAs per SM");
   const unsigned long long ctas = static_cast<unsigned long long>(p.num_q_tiles) * p.num_seqs *
                                   (p.verify ? p.num_kv_heads : p.num_qo_heads);
   if (ctas == 0) return cudaSuccess;
   if (ctas > 0x7fffffffull) return cudaErrorInvalidConfiguration;
-  if (p.verify) return launch_prefill_variant<true, true>(qmap, kmap, vmap, p, static_cast<unsigned>(ctas), stream);
-  if (p.paged) return launch_prefill_variant<true, false>(qmap, kmap, vmap, p, static_cast<unsigned>(ctas), stream);
-  return launch_prefill_variant<false, false>(qmap, kmap, vmap, p, static_cast<unsigned>(ctas), stream);
+  if (p.verify) return launch_prefill_variant<true, true>(qmap, kmap, vmap, p, static_cast<unsigned>(ctas), stream, programmatic);
+  if (p.paged) return launch_prefill_variant<true, false>(qmap, kmap, vmap, p, static_cast<unsigned>(ctas), stream, false);
+  return launch_prefill_variant<false, false>(qmap, kmap, vmap, p, static_cast<unsigned>(ctas), stream, false);
 }
 
 }  // namespace sa

@@ -205,7 +205,13 @@ size_t decode_counter_bytes(int batch, int num_qo_heads, int num_kv_heads, int q
   return (units * sizeof(int) + 255) & ~size_t(255);
 }
 std::atomic<int> g_programmatic{0};
-bool programmatic_launch() { return g_programmatic.load(std::memory_order_relaxed) != 0; }
+
+// Launch mode of one call: its own flag, else the process-wide default.
+bool programmatic_for(int launch_flags) {
+  if (launch_flags == SINKATTN_LAUNCH_PROGRAMMATIC) return true;
+  if (launch_flags == SINKATTN_LAUNCH_PLAIN) return false;
+  return g_programmatic.load(std::memory_order_relaxed) != 0;
+}
 
 }  // namespace sa
 
@@ -222,10 +228,20 @@ const char *sinkattn_status_string(int status) {
   }
 }
 
-int sinkattn_version(void) { return 300; }   // 0.3.0: programmatic dependent launch
+int sinkattn_version(void) { return 400; }   // 0.4.0: launch mode per call
 
 int sinkattn_set_programmatic_launch(int enable) {
   return sa::g_programmatic.exchange(enable != 0 ? 1 : 0);
+}
+
+size_t sinkattn_decode_workspace_bytes(int batch, int num_qo_heads, int head_dim, int num_splits) {
+  if (batch <= 0 || num_qo_heads <= 0 || head_dim != kHeadDim || num_splits <= 1) return 0;
+  // counters: one int per (request, KV head, 8-head block) <= one per
+  // (request, query head), whatever the KV head count; then the chunk slots
+  const size_t counters = (static_cast<size_t>(batch) * num_qo_heads * sizeof(int) + 255) &
+                          ~size_t(255);
+  const size_t rows = static_cast<size_t>(num_splits) * batch * num_qo_heads;
+  return counters + rows * kHeadDim * sizeof(float) + ((rows * sizeof(float) + 255) & ~size_t(255));
 }
 
 const char *sinkattn_last_error(void) { return g_last_error; }
@@ -269,15 +285,18 @@ int sinkattn_verify_plan(int batch, int q_len, int num_qo_heads, int num_kv_head
 
 }  // extern "C"
 
-namespace {
+namespace sa {
 
 // Decode of q_len tokens per request; q_len = 1 with no mask is plain decode.
-int decode_common(const void *q, const void *k_cache, const void *v_cache,
-                  const int32_t *page_table, int max_pages_per_seq, const int32_t *kv_lens,
-                  const uint64_t *tree_mask, const float *sinks, float scale, void *out, float *lse,
-                  int batch, int q_len, int num_qo_heads, int num_kv_heads, int head_dim,
-                  int page_size, int num_pages, int max_kv_len, int num_splits, void *workspace,
-                  size_t workspace_bytes, void *stream) {
+int decode_entry(const void *q, const void *k_cache, const void *v_cache,
+                 const int32_t *page_table, int max_pages_per_seq, const int32_t *kv_lens,
+                 const uint64_t *tree_mask, const float *sinks, float scale, void *out, float *lse,
+                 int batch, int q_len, int num_qo_heads, int num_kv_heads, int head_dim,
+                 int page_size, int num_pages, int max_kv_len, int num_splits, void *workspace,
+                 size_t workspace_bytes, int launch_flags, bool zero_counters, void *stream) {
+  if (launch_flags != SINKATTN_LAUNCH_DEFAULT && launch_flags != SINKATTN_LAUNCH_PLAIN &&
+      launch_flags != SINKATTN_LAUNCH_PROGRAMMATIC)
+    return SINKATTN_INVALID_ARGUMENT;
   if (head_dim != kHeadDim || page_size != kPageSize) return SINKATTN_UNSUPPORTED;
   if (batch < 0 || q_len < 1 || q_len > SINKATTN_MAX_VERIFY_TOKENS || num_qo_heads <= 0 ||
       num_kv_heads <= 0 || num_qo_heads % num_kv_heads || max_kv_len < 0 || num_splits < 0 ||
@@ -304,6 +323,8 @@ int decode_common(const void *q, const void *k_cache, const void *v_cache,
     if (!workspace || workspace_bytes < plan.workspace_bytes) return SINKATTN_WORKSPACE_TOO_SMALL;
     if (!aligned(workspace, 256)) return SINKATTN_INVALID_ARGUMENT;
   }
+  const bool programmatic = programmatic_for(launch_flags);
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   if (plan.tensor_cores) {
     // query rows (token, head) of a KV head: box {64, group, 128 / group}
@@ -335,7 +356,7 @@ int decode_common(const void *q, const void *k_cache, const void *v_cache,
     pp.num_q_tiles = ceil_div(q_len, kPrefillTile / group);
     pp.verify = 1;
     pp.tree_mask = tree_mask;
-    return cuda_status(sa::launch_prefill(qmap, kmap, vmap, pp, static_cast<cudaStream_t>(stream)),
+    return cuda_status(launch_prefill(qmap, kmap, vmap, pp, st, programmatic),
                        "verification launch");
   }
 
@@ -373,11 +394,16 @@ int decode_common(const void *q, const void *k_cache, const void *v_cache,
   p.num_splits = plan.num_splits;
   p.pages_per_chunk = plan.pages_per_chunk;
   p.sorted_dispatch = plan.sorted_dispatch;
-  return cuda_status(sa::launch_decode(kmap, vmap, p, static_cast<cudaStream_t>(stream)),
-                     "decode launch");
+  if (zero_counters && plan.num_splits > 1) {
+    // the counters are the workspace's first plan.counters_bytes bytes, all
+    // within workspace_bytes (checked above)
+    const cudaError_t e = cudaMemsetAsync(workspace, 0, plan.counters_bytes, st);
+    if (e != cudaSuccess) return cuda_status(e, "merge counter clear");
+  }
+  return cuda_status(launch_decode(kmap, vmap, p, st, programmatic), "decode launch");
 }
 
-}  // namespace
+}  // namespace sa
 
 extern "C" {
 
@@ -387,9 +413,22 @@ int sinkattn_decode(const void *q, const void *k_cache, const void *v_cache,
                     int num_qo_heads, int num_kv_heads, int head_dim, int page_size, int num_pages,
                     int max_kv_len, int num_splits, void *workspace, size_t workspace_bytes,
                     void *stream) {
-  return decode_common(q, k_cache, v_cache, page_table, max_pages_per_seq, kv_lens, nullptr, sinks,
-                       scale, out, lse, batch, 1, num_qo_heads, num_kv_heads, head_dim, page_size,
-                       num_pages, max_kv_len, num_splits, workspace, workspace_bytes, stream);
+  return sa::decode_entry(q, k_cache, v_cache, page_table, max_pages_per_seq, kv_lens, nullptr,
+                         sinks, scale, out, lse, batch, 1, num_qo_heads, num_kv_heads, head_dim,
+                         page_size, num_pages, max_kv_len, num_splits, workspace, workspace_bytes,
+                         SINKATTN_LAUNCH_DEFAULT, false, stream);
+}
+
+int sinkattn_decode_ex(const void *q, const void *k_cache, const void *v_cache,
+                       const int32_t *page_table, int max_pages_per_seq, const int32_t *kv_lens,
+                       const float *sinks, float scale, void *out, float *lse, int batch,
+                       int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
+                       int num_pages, int max_kv_len, int num_splits, void *workspace,
+                       size_t workspace_bytes, int launch_flags, void *stream) {
+  return sa::decode_entry(q, k_cache, v_cache, page_table, max_pages_per_seq, kv_lens, nullptr,
+                         sinks, scale, out, lse, batch, 1, num_qo_heads, num_kv_heads, head_dim,
+                         page_size, num_pages, max_kv_len, num_splits, workspace, workspace_bytes,
+                         launch_flags, false, stream);
 }
 
 int sinkattn_verify(const void *q, const void *k_cache, const void *v_cache,
@@ -398,10 +437,22 @@ int sinkattn_verify(const void *q, const void *k_cache, const void *v_cache,
                     float *lse, int batch, int q_len, int num_qo_heads, int num_kv_heads,
                     int head_dim, int page_size, int num_pages, int max_kv_len, int num_splits,
                     void *workspace, size_t workspace_bytes, void *stream) {
-  return decode_common(q, k_cache, v_cache, page_table, max_pages_per_seq, kv_lens, tree_mask,
-                       sinks, scale, out, lse, batch, q_len, num_qo_heads, num_kv_heads, head_dim,
-                       page_size, num_pages, max_kv_len, num_splits, workspace, workspace_bytes,
-                       stream);
+  return sa::decode_entry(q, k_cache, v_cache, page_table, max_pages_per_seq, kv_lens, tree_mask,
+                         sinks, scale, out, lse, batch, q_len, num_qo_heads, num_kv_heads,
+                         head_dim, page_size, num_pages, max_kv_len, num_splits, workspace,
+                         workspace_bytes, SINKATTN_LAUNCH_DEFAULT, false, stream);
+}
+
+int sinkattn_verify_ex(const void *q, const void *k_cache, const void *v_cache,
+                       const int32_t *page_table, int max_pages_per_seq, const int32_t *kv_lens,
+                       const uint64_t *tree_mask, const float *sinks, float scale, void *out,
+                       float *lse, int batch, int q_len, int num_qo_heads, int num_kv_heads,
+                       int head_dim, int page_size, int num_pages, int max_kv_len, int num_splits,
+                       void *workspace, size_t workspace_bytes, int launch_flags, void *stream) {
+  return sa::decode_entry(q, k_cache, v_cache, page_table, max_pages_per_seq, kv_lens, tree_mask,
+                         sinks, scale, out, lse, batch, q_len, num_qo_heads, num_kv_heads,
+                         head_dim, page_size, num_pages, max_kv_len, num_splits, workspace,
+                         workspace_bytes, launch_flags, false, stream);
 }
 
 int sinkattn_prefill(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
@@ -440,7 +491,8 @@ int sinkattn_prefill(const void *q, const void *k, const void *v, const int32_t 
   p.group = num_qo_heads / num_kv_heads;
   p.paged = 0;
   p.num_q_tiles = ceil_div(max_seqlen, kPrefillTile);
-  return cuda_status(sa::launch_prefill(qmap, kmap, vmap, p, static_cast<cudaStream_t>(stream)),
+  return cuda_status(sa::launch_prefill(qmap, kmap, vmap, p, static_cast<cudaStream_t>(stream),
+                                        false),
                      "prefill launch");
 }
 
@@ -489,7 +541,8 @@ int sinkattn_prefill_paged(const void *q, const int32_t *cu_seqlens_q, int num_s
   p.num_pages = num_pages;
   p.paged = 1;
   p.num_q_tiles = ceil_div(max_q_len, kPrefillTile);
-  return cuda_status(sa::launch_prefill(qmap, kmap, vmap, p, static_cast<cudaStream_t>(stream)),
+  return cuda_status(sa::launch_prefill(qmap, kmap, vmap, p, static_cast<cudaStream_t>(stream),
+                                        false),
                      "prefill launch");
 }
 

@@ -38,8 +38,9 @@
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *     default stream), never synchronises, allocates nothing, and keeps no
  *     state beyond per-device caches (the SM count, kernel attributes set
- *     once) and the process-wide launch mode of
- *     sinkattn_set_programmatic_launch.  Calls are thread-safe.
+ *     once) and the process-wide default launch mode of
+ *     sinkattn_set_programmatic_launch, which the _ex entry points override
+ *     per call.  Calls are thread-safe.
  *   - Return value: a sinkattn_status.  Argument checks happen on the host
  *     before any launch; SINKATTN_CUDA_ERROR reports a launch failure.
  */
@@ -78,10 +79,26 @@ SINKATTN_API const char *sinkattn_last_error(void);
 SINKATTN_API int sinkattn_version(void);
 
 /*
+ * Launch modes of the decode and verification kernels, chosen per call by
+ * the launch_flags argument of sinkattn_decode_ex and sinkattn_verify_ex:
+ *   SINKATTN_LAUNCH_DEFAULT       the process-wide default below
+ *   SINKATTN_LAUNCH_PLAIN         an ordinary launch: the kernel starts after
+ *                                 everything before it on the stream
+ *   SINKATTN_LAUNCH_PROGRAMMATIC  programmatic dependent launch (below)
+ * Any other value returns SINKATTN_INVALID_ARGUMENT without launching.
+ */
+#define SINKATTN_LAUNCH_DEFAULT 0
+#define SINKATTN_LAUNCH_PLAIN 1
+#define SINKATTN_LAUNCH_PROGRAMMATIC 2
+
+/*
  * Programmatic dependent launch of the decode and verification kernels
- * (sinkattn_decode, sinkattn_decode_static_scratch and both routes of
- * sinkattn_verify; prefill is unaffected).  Process-wide, off by default;
- * returns the previous setting.  When on, such a kernel may be scheduled
+ * (sinkattn_decode, sinkattn_decode_static_scratch, both routes of
+ * sinkattn_verify, and the _ex entry points given SINKATTN_LAUNCH_DEFAULT;
+ * prefill is unaffected).  This sets the process-wide DEFAULT, off at load;
+ * returns the previous setting.  A caller that shares the process with other
+ * users of the library should pass its mode per call (the _ex entry points)
+ * instead of changing the default.  In programmatic mode a kernel may be scheduled
  * while the kernel launched before it on the same stream is still running:
  * its CTAs rank the requests (kv_lens), read their first page ids
  * (page_table) and set up shared and tensor memory, then wait for the
@@ -92,8 +109,9 @@ SINKATTN_API int sinkattn_version(void);
  * as soon as all of its own CTAs have started.
  * Caller's contract while it is on: kv_lens and page_table of a call are not
  * written by the kernel launched immediately before the call on its stream
- * (they may come from host copies, memsets or any earlier kernel).  Launches
- * inside CUDA graph capture keep the same ordering.
+ * (they may come from host copies, memsets or any earlier kernel).  A
+ * violation is not detected: the kernel may read the old kv_lens or page
+ * table.  Launches inside CUDA graph capture keep the same ordering.
  */
 SINKATTN_API int sinkattn_set_programmatic_launch(int enable);
 
@@ -112,6 +130,21 @@ SINKATTN_API int sinkattn_set_programmatic_launch(int enable);
 SINKATTN_API int sinkattn_decode_plan(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
                          int page_size, int max_kv_len, int num_sms,
                          int *num_splits, size_t *workspace_bytes);
+
+/*
+ * Upper bound on the workspace sinkattn_decode needs with an explicit split
+ * count num_splits, for any num_kv_heads that divides num_qo_heads and any
+ * kv lengths (host only).  The merge counters take at most one int per
+ * (request, query head), 256-byte rounded; each split then holds an fp32 row
+ * of head_dim and an fp32 lse per (request, query head), the lse block
+ * 256-byte rounded.  Returns 0 for num_splits <= 1 (no workspace), for
+ * batch <= 0 or num_qo_heads <= 0, and for head_dim != 64.  The plan may use
+ * fewer splits than requested (at most one page per chunk), never more, so
+ * the bound always suffices; sinkattn_decode_plan gives the exact figure,
+ * including the split count that num_splits = 0 (choose) leads to.
+ */
+SINKATTN_API size_t sinkattn_decode_workspace_bytes(int batch, int num_qo_heads, int head_dim,
+                                        int num_splits);
 
 /*
  * Decode: one new query token per request against its paged KV.
@@ -148,6 +181,17 @@ SINKATTN_API int sinkattn_decode(const void *q, const void *k_cache, const void 
                     int batch, int num_qo_heads, int num_kv_heads, int head_dim,
                     int page_size, int num_pages, int max_kv_len, int num_splits,
                     void *workspace, size_t workspace_bytes, void *stream);
+
+/* sinkattn_decode with the launch mode chosen by this call (launch_flags =
+ * SINKATTN_LAUNCH_*), whatever the process-wide default. */
+SINKATTN_API int sinkattn_decode_ex(const void *q, const void *k_cache, const void *v_cache,
+                    const int32_t *page_table, int max_pages_per_seq,
+                    const int32_t *kv_lens, const float *sinks, float scale,
+                    void *out, float *lse,
+                    int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                    int page_size, int num_pages, int max_kv_len, int num_splits,
+                    void *workspace, size_t workspace_bytes, int launch_flags,
+                    void *stream);
 
 /*
  * Verification of draft tokens ("Accelerating Sonar through speculation",
@@ -192,6 +236,17 @@ SINKATTN_API int sinkattn_verify(const void *q, const void *k_cache, const void 
                     int head_dim, int page_size, int num_pages, int max_kv_len,
                     int num_splits, void *workspace, size_t workspace_bytes,
                     void *stream);
+
+/* sinkattn_verify with the launch mode chosen by this call (launch_flags =
+ * SINKATTN_LAUNCH_*), whatever the process-wide default. */
+SINKATTN_API int sinkattn_verify_ex(const void *q, const void *k_cache, const void *v_cache,
+                    const int32_t *page_table, int max_pages_per_seq,
+                    const int32_t *kv_lens, const uint64_t *tree_mask,
+                    const float *sinks, float scale, void *out, float *lse,
+                    int batch, int q_len, int num_qo_heads, int num_kv_heads,
+                    int head_dim, int page_size, int num_pages, int max_kv_len,
+                    int num_splits, void *workspace, size_t workspace_bytes,
+                    int launch_flags, void *stream);
 
 /*
  * Causal prefill over ragged sequences packed along the token axis.
@@ -303,14 +358,20 @@ SINKATTN_API int sinkattn_qkv_prologue(const void *qkv, const void *bias,
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
  *     that first call before any stream capture on the device.
- *   - Returns SINKATTN_WORKSPACE_TOO_SMALL, launching nothing, when the plan
- *     for these sizes (see sinkattn_decode_plan) needs more scratch than the
- *     array holds.  Passing num_splits = 1 needs no scratch at all.
+ *   - Every argument check of sinkattn_decode runs first; a refused call
+ *     queues no work on the stream.  Returns SINKATTN_WORKSPACE_TOO_SMALL,
+ *     launching nothing, when the plan for these sizes (see
+ *     sinkattn_decode_plan) needs more scratch than the array holds.
+ *   - A plan with one split (num_splits = 1, or a chosen plan that keeps
+ *     whole requests) neither reads nor writes the array.
  *   - All calls share the one array, and it keeps the last call's contents.
- *     Each call first clears the part that must start at zero (the merge
- *     counters, with cudaMemsetAsync on `stream`); two calls that overlap on
- *     the GPU (different streams, or different host threads, without
- *     ordering between them) race on the array and may return wrong results.
+ *     A call whose plan has more than one split first clears the part that
+ *     must start at zero (the merge counters, with cudaMemsetAsync on
+ *     `stream`); two such calls that overlap on the GPU (different streams,
+ *     or different host threads, without ordering between them) race on the
+ *     array and may return wrong results.
+ *   - The launch mode is the process-wide default
+ *     (sinkattn_set_programmatic_launch).
  */
 #define SINKATTN_STATIC_SCRATCH_BYTES (16u << 20)
 

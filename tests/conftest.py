@@ -25,3 +25,19 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """With SINKATTN_PARITY_REPORT=<path>, write every oracle comparison the
+    session made (per test: elements, max error, |ref| >= 4 count, elements
+    passed by the one-ulp rule) to <path> as JSON."""
+    path = os.environ.get("SINKATTN_PARITY_REPORT")
+    if not path:
+        return
+    import json
+    try:
+        import tolerances
+    except ImportError:
+        return
+    with open(path, "w") as f:
+        json.dump(tolerances.RECORD, f, indent=1, sort_keys=True)

@@ -104,6 +104,39 @@ def test_decode_rejects_on_host(lib):
     assert _raw_decode(lib, batch=1, hq=65536 * 8, hkv=65536, **ok) == sa.UNSUPPORTED
 
 
+def test_decode_ex_rejects_unknown_launch_flags_on_host(lib):
+    # the flags are checked before anything else, so no device is needed
+    args = [None, None, None, None, 1, None, None, 0.125, None, None, 1, 8, 1, 64, 16, 1, 16, 0,
+            None, 0]
+    for flags in (-1, 3, 7):
+        assert lib.sinkattn_decode_ex(*args, flags, None) == sa.INVALID_ARGUMENT
+    vargs = [None, None, None, None, 1, None, None, None, 0.125, None, None, 1, 2, 8, 1, 64, 16,
+             1, 16, 0, None, 0]
+    assert lib.sinkattn_verify_ex(*vargs, 3, None) == sa.INVALID_ARGUMENT
+    # a valid mode goes on to the ordinary checks (null pointers here)
+    for flags in (sa.LAUNCH_DEFAULT, sa.LAUNCH_PLAIN, sa.LAUNCH_PROGRAMMATIC):
+        assert lib.sinkattn_decode_ex(*args, flags, None) == sa.INVALID_ARGUMENT
+        assert lib.sinkattn_decode_ex(*args[:13], 128, *args[14:], flags,
+                                      None) == sa.UNSUPPORTED
+
+
+@pytest.mark.parametrize("batch,hq", [(1, 1), (8, 64), (64, 64), (3, 40), (1000, 128)])
+def test_decode_workspace_bytes_bounds_every_plan(lib, batch, hq):
+    assert sa.decode_workspace_bytes(batch, hq, 0) == 0
+    assert sa.decode_workspace_bytes(batch, hq, 1) == 0
+    assert sa.decode_workspace_bytes(batch, hq, 4, head_dim=128) == 0
+    for splits in (2, 3, 8, 64, 1024):
+        bound = sa.decode_workspace_bytes(batch, hq, splits)
+        assert bound > 0 and bound % 256 == 0
+        for hkv in [h for h in (1, 2, 4, 8, 16, 40, 64, 128) if h <= hq and hq % h == 0]:
+            for max_kv in (16, 700, 4096, 131072):
+                s, ws = sa.decode_plan(batch, hq, hkv, max_kv, num_splits=splits, num_sms=152)
+                assert s <= splits and ws <= bound, (splits, hkv, max_kv, s, ws, bound)
+    # with group 1 the counters take one int per (request, head): the bound is exact
+    s, ws = sa.decode_plan(batch, hq, hq, 1 << 20, num_splits=8, num_sms=152)
+    assert s == 8 and ws == sa.decode_workspace_bytes(batch, hq, 8)
+
+
 def test_programmatic_launch_switch_is_host_state(lib):
     prev = sa.set_programmatic_launch(True)
     try:

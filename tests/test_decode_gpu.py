@@ -80,6 +80,26 @@ def test_long_context_split_decode(splits):
     assert_lse_close(lse, rl)
 
 
+def test_mixed_batch_decode_part():
+    """The mixed serving batch's decode half: 32 requests with kv_len in
+    [512, 16384] in the page pool they share with the four extend requests
+    (shuffled pages, NaN-filled spares), the planner's own split choice (fewer
+    (request, KV head) units than one wave, so chunked split-KV with the
+    in-kernel merge), all 32 requests x 64 heads against the oracle."""
+    m = workloads.mixed_batch()
+    d = m["decode"]
+    splits, ws = sa.decode_plan(32, 64, 8, d["max_kv_len"])
+    assert splits > 1 and ws > 0                  # the split path with its merge
+    w = dict(q=d["q"], k_cache=m["k_cache"], v_cache=m["v_cache"], page_table=d["page_table"],
+             kv_lens=d["kv_lens"], sinks=m["sinks"], scale=m["scale"],
+             max_kv_len=d["max_kv_len"])
+    ro, rl = ref_decode(w)
+    for _ in range(2):                            # the counters reset: a second call agrees
+        out, lse = run_decode(w)
+        assert_out_close(out, ro, "mixed decode out")
+        assert_lse_close(lse, rl, "mixed decode lse")
+
+
 EDGE_LENS = [0, 1, 2, 15, 16, 17, 31, 32, 33, 63, 64, 65, 100, 255, 256, 257, 1000]
 
 

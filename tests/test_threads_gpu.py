@@ -1,8 +1,9 @@
 """Concurrent host threads: the C ABI promises thread-safe calls (its only
-state is per-device caches and the launch-mode switch).  Four threads, each
+state is per-device caches and the default launch mode).  Four threads, each
 on its own stream, run decode (a split plan with its own workspace) and
 tensor-core verification back to back; every result must equal the same call
-made alone, bit for bit, in both launch modes."""
+made alone, bit for bit, in both launch modes.  Threads that pick different
+launch modes per call do not affect one another."""
 
 import threading
 
@@ -67,5 +68,59 @@ def test_concurrent_threads_match_single_calls(programmatic):
         for got in results:
             for a, b in zip(got, ref):
                 assert torch.equal(_bits(a), _bits(b))
+    finally:
+        sa.set_programmatic_launch(prev)
+
+
+def test_threads_with_their_own_launch_modes():
+    # one thread launches programmatically, the other plainly, each chaining
+    # decode -> decode (q = the previous output) and a tensor-core
+    # verification on its own stream, while the process-wide default stays
+    # off; both must equal the same chain made one call at a time
+    dw = _dev(workloads.decode_batch(seed=23, batch=16, min_len=2000, max_len=6000))
+    vw = _dev(workloads.verify_batch(seed=24, batch=64, q_len=4, max_len=1500))
+    assert sa.decode_plan(16, 64, 8, dw["max_kv_len"])[0] > 1
+
+    def chain(mode, stream=None):
+        q, got = dw["q"], []
+        for _ in range(6):
+            out, lse = sa.decode(q, dw["k_cache"], dw["v_cache"], dw["page_table"],
+                                 dw["kv_lens"], dw["sinks"], dw["scale"], dw["max_kv_len"],
+                                 stream=stream, programmatic=mode)
+            got += [out, lse]
+            q = out
+        got += list(sa.verify(vw["q"], vw["k_cache"], vw["v_cache"], vw["page_table"],
+                              vw["kv_lens"], vw["sinks"], vw["scale"], vw["max_kv_len"],
+                              stream=stream, programmatic=mode))
+        return got
+
+    prev = sa.set_programmatic_launch(False)
+    try:
+        ref = chain(False)
+        torch.cuda.synchronize()
+        results, errors = {}, []
+
+        def worker(mode):
+            try:
+                torch.cuda.set_device(0)
+                s = torch.cuda.Stream()
+                with torch.cuda.stream(s):
+                    for _ in range(5):
+                        got = chain(mode, s)
+                s.synchronize()
+                results[mode] = got
+            except Exception as exc:                # reported on the main thread
+                errors.append(exc)
+
+        threads = [threading.Thread(target=worker, args=(m,)) for m in (True, False)]
+        for t in threads:
+            t.start()
+        for t in threads:
+            t.join()
+        assert not errors, errors
+        assert sa.set_programmatic_launch(False) is False    # the default never changed
+        for mode in (True, False):
+            for a, b in zip(results[mode], ref):
+                assert torch.equal(_bits(a), _bits(b)), mode
     finally:
         sa.set_programmatic_launch(prev)
