@@ -771,6 +771,77 @@ def run_mixed(args, rank, dev, peaks):
                 combined_roofline_frac=round(ideal / (t_all / steps), 4))
 
 
+def run_gqa(args, rank, dev, peaks):
+    """Decode over GQA group sizes (query / KV heads 64/8, 48/4, 64/4, 128/8,
+    64/2) at 64 and 128 requests, kv_len U[1,4096]: groups above 8 run 16
+    heads per CTA when those CTAs fill a wave."""
+    import torch
+
+    import gqa_attention_learned_gb300 as sa
+    from gqa_attention_learned_gb300 import workloads
+
+    res = {}
+    for hq, hkv, b in ((64, 8, 64), (48, 4, 64), (64, 4, 64), (64, 4, 128), (128, 8, 64),
+                       (64, 2, 64)):
+        w = workloads.decode_batch(seed=1 + 1000 * rank, batch=b, num_qo_heads=hq,
+                                   num_kv_heads=hkv)
+        nbytes = decode_bytes([int(x) for x in w["kv_lens"]], hq, hkv)
+        q = w["q"].to(dev)
+        pools = [(w["k_cache"].to(dev), w["v_cache"].to(dev))]
+        pools.append((pools[0][0].clone(), pools[0][1].clone()))
+        table, lens, sinks = w["page_table"].to(dev), w["kv_lens"].to(dev), w["sinks"].to(dev)
+        splits, ws_bytes = sa.decode_plan(b, hq, hkv, w["max_kv_len"])
+        ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+        stream = torch.cuda.current_stream()
+        run = {"splits": splits}
+        for mode in (True, False):
+            def step(i, mode=mode, q=q, pools=pools, table=table, lens=lens, sinks=sinks, w=w,
+                     ws=ws):
+                kc, vc = pools[i & 1]
+                sa.decode(q, kc, vc, table, lens, sinks, w["scale"], w["max_kv_len"],
+                          workspace=ws, stream=stream, programmatic=mode)
+            steps = max(50, args.steps // 20)
+            secs = _time_steps(torch, step, steps, args.warmup, stream)
+            _, _, bps = aggregate(nbytes * steps, secs, dev)
+            key = "programmatic" if mode else "plain"
+            run[key] = round(bps / 1e9, 1)
+            run[key + "_frac"] = round(bps / 1e9 / peaks["hbm_gbs"], 4)
+        res[f"{hq} q / {hkv} kv heads, {b} requests"] = run
+        del pools, q
+        torch.cuda.empty_cache()
+    return dict(workload="decode, kv_len U[1,4096], bf16 paged KV (page 16, shuffled), two KV "
+                         "pool copies alternate", runs=res)
+
+
+SECTIONS = {"long": "long_decode", "graph": "graph_decode", "verify": "verify",
+            "prologue": "prologue", "prefill": "prefill", "mixed": "mixed", "gqa": "gqa"}
+
+
+def only_section(args):
+    """One extra section alone (no headline decode, no CPU baseline): its
+    figures as one JSON line, for profiling a single kernel's workload."""
+    import torch
+
+    world, rank, local = dist_info()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist_init("nccl" if world > 1 else "gloo")
+    import gqa_attention_learned_gb300 as sa
+    sa.load()
+    sa.set_programmatic_launch(not args.plain_launch)
+    peaks, _ = load_peaks()
+    fn = {"long": lambda: run_long_decode(args, rank, dev),
+          "graph": lambda: run_graph_decode(args, rank, dev, peaks),
+          "verify": lambda: run_verify(args, rank, dev, peaks),
+          "prologue": lambda: run_prologue(args, rank, dev, peaks),
+          "prefill": lambda: run_prefill(args, rank, dev, peaks),
+          "mixed": lambda: run_mixed(args, rank, dev, peaks),
+          "gqa": lambda: run_gqa(args, rank, dev, peaks)}[args.only]
+    out = fn()
+    if rank == 0:
+        print(json.dumps({"section": SECTIONS[args.only], **out}), flush=True)
+
+
 def section_summary(extra, peaks):
     """Flat numeric figures of the extra sections (GB/s, TFLOP/s and
     fractions of the measured peaks) for the printed line; the full sections
@@ -842,6 +913,8 @@ def gpu_arm(args):
             extra["prefill"] = run_prefill(args, rank, dev, peaks)
         if "mixed" in sections:
             extra["mixed"] = run_mixed(args, rank, dev, peaks)
+        if "gqa" in sections:
+            extra["gqa"] = run_gqa(args, rank, dev, peaks)
     roofline = {"bound": "hbm", "achieved": round(kernel_gbps, 2), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(kernel_gbps / peaks["hbm_gbs"], 4),
                 "traffic": kernel_traffic("decode"), "peak_source": peak_src,
@@ -1000,6 +1073,8 @@ def main():
                     help="launch decode kernels without programmatic dependent launch")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--only", choices=sorted(SECTIONS), default=None,
+                    help="run one extra section alone and print its figures (profiling)")
     ap.add_argument("--details", default=None,
                     help="write the full sections (e2e variants, per-run figures) to this JSON file")
     ap.add_argument("--oracle-worker", default=None, help=argparse.SUPPRESS)
@@ -1011,6 +1086,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         reference_arm(args)
+    elif args.only:
+        only_section(args)
     else:
         gpu_arm(args)
 

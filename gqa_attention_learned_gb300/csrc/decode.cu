@@ -7,7 +7,9 @@
 // started at -inf, blocks merged by log-sum-exp.
 //
 // Design (GB300, HBM-bound):
-//  * One CTA = one (request, KV head, 8-query-head block, KV chunk).  When
+//  * One CTA = one (request, KV head, block of 8 or 16 query heads, KV
+//    chunk): a GQA group above 8 takes two 8-head column blocks per CTA, so
+//    every page is read once per 16 heads.  When
 //    the plan has one chunk per request the requests are dispatched heaviest
 //    first (by size class, computed from kv_lens in every CTA) so that the
 //    last wave holds the short ones.  Its
@@ -625,7 +627,10 @@ cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap, cons
                           cudaStream_t stream, bool programmatic) {
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
   const bool verify = p.q_len > 1 || p.tree_mask != nullptr;
-  if (!verify && p.col_blocks == 1) return launch_variant<1, false>(kmap, vmap, p, stream, programmatic);
+  if (!verify) {
+    return p.col_blocks == 1 ? launch_variant<1, false>(kmap, vmap, p, stream, programmatic)
+                             : launch_variant<2, false>(kmap, vmap, p, stream, programmatic);
+  }
   if (p.col_blocks == 1) return launch_variant<1, true>(kmap, vmap, p, stream, programmatic);
   return launch_variant<2, true>(kmap, vmap, p, stream, programmatic);
 }

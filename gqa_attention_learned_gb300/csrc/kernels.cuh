@@ -85,8 +85,6 @@ inline int decode_col_blocks(int rows) { return rows > 8 ? 2 : 1; }
 int decode_ctas_per_sm();
 // Largest split count.
 int decode_max_splits();
-// Bytes at the start of the decode workspace that must be zero before a call.
-size_t decode_counter_bytes(int batch, int num_qo_heads, int num_kv_heads, int q_len = 1);
 
 // `programmatic`: launch with the programmatic-serialization attribute (the
 // kernel waits for the previous kernel on the stream before touching anything

@@ -170,8 +170,11 @@ SINKATTN_API size_t sinkattn_decode_workspace_bytes(int batch, int num_qo_heads,
  * Long contexts run as num_splits KV chunks per (request, KV head), the sink
  * entering chunk 0 only; the last chunk to finish merges them by
  * log-sum-exp inside the same kernel.
- * Limits: batch <= 65535, and num_kv_heads times the 8-row query blocks per
- * KV head (ceil(group / 8) for decode) <= 65535; larger calls return
+ * Query heads of a KV head go to CTAs 8 at a time, or 16 at a time when a
+ * KV head has more than 8 (a GQA group above 8), so each CTA reads each page
+ * once for all of its heads.
+ * Limits: batch <= 65535, and num_kv_heads times the CTAs per KV head
+ * (ceil(group / 16) for groups above 8, else 1) <= 65535; larger calls return
  * SINKATTN_UNSUPPORTED without launching.
  */
 SINKATTN_API int sinkattn_decode(const void *q, const void *k_cache, const void *v_cache,

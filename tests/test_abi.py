@@ -137,6 +137,34 @@ def test_decode_workspace_bytes_bounds_every_plan(lib, batch, hq):
     assert s == 8 and ws == sa.decode_workspace_bytes(batch, hq, 8)
 
 
+def _counter_bytes(units):
+    return (units * 4 + 255) // 256 * 256
+
+
+def _split_workspace(batch, hq, splits, counters_units):
+    rows = splits * batch * hq
+    return _counter_bytes(counters_units) + rows * 64 * 4 + (rows * 4 + 255) // 256 * 256
+
+
+def test_plan_takes_16_head_ctas_when_they_fill_a_wave(lib):
+    # 2 CTAs per SM x 152 SMs = 304 slots.  GQA group 16 (32 q / 2 KV heads):
+    # 160 requests give 320 (request, KV head) units of 16 heads, a full
+    # wave, so one merge counter per unit; 100 requests give 200, so the plan
+    # keeps 8-head CTAs (two per unit, two counters)
+    s, ws = sa.decode_plan(160, 32, 2, 4096, num_splits=2, num_sms=152)
+    assert s == 2 and ws == _split_workspace(160, 32, 2, 160 * 2)
+    s, ws = sa.decode_plan(100, 32, 2, 4096, num_splits=2, num_sms=152)
+    assert s == 2 and ws == _split_workspace(100, 32, 2, 100 * 2 * 2)
+    # group 32: two 16-head CTAs per KV head when wide, four 8-head ones when not
+    s, ws = sa.decode_plan(80, 64, 2, 4096, num_splits=2, num_sms=152)
+    assert ws == _split_workspace(80, 64, 2, 80 * 2 * 2)
+    s, ws = sa.decode_plan(40, 64, 2, 4096, num_splits=2, num_sms=152)
+    assert ws == _split_workspace(40, 64, 2, 40 * 2 * 4)
+    # groups of 8 or less always use 8-head CTAs
+    s, ws = sa.decode_plan(400, 64, 8, 4096, num_splits=2, num_sms=152)
+    assert ws == _split_workspace(400, 64, 2, 400 * 8)
+
+
 def test_programmatic_launch_switch_is_host_state(lib):
     prev = sa.set_programmatic_launch(True)
     try:

@@ -100,6 +100,22 @@ def test_mixed_batch_decode_part():
         assert_lse_close(lse, rl, "mixed decode lse")
 
 
+@pytest.mark.parametrize("hq,hkv,batch", [(32, 2, 160), (48, 4, 80), (64, 2, 80), (128, 8, 40)])
+@pytest.mark.parametrize("splits", [0, 3])
+def test_wide_gqa_groups(hq, hkv, batch, splits):
+    """GQA groups above 8 (12, 16, 32) with enough requests that the plan
+    takes 16-head CTAs (each page read once for 16 heads): whole requests
+    heaviest first, and an explicit 3-way split with its merge; kv_len 0..900
+    with a few empty requests."""
+    w = workloads.decode_batch(seed=hq + hkv + batch + splits, batch=batch, num_qo_heads=hq,
+                               num_kv_heads=hkv, min_len=0, max_len=900)
+    assert int(w["kv_lens"].min()) >= 0
+    out, lse = run_decode(w, num_splits=splits)
+    ro, rl = ref_decode(w)
+    assert_out_close(out, ro)
+    assert_lse_close(lse, rl)
+
+
 EDGE_LENS = [0, 1, 2, 15, 16, 17, 31, 32, 33, 63, 64, 65, 100, 255, 256, 257, 1000]
 
 
