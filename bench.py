@@ -49,11 +49,11 @@ TRAFFIC = {
     "decode": {"sources": ("gqa_attention_learned_gb300/csrc/decode.cu",
                            "gqa_attention_learned_gb300/csrc/kernels.cuh",
                            "gqa_attention_learned_gb300/csrc/ptx.cuh"),
-               "sha256_16": None, "bytes": None},
+               "sha256_16": "ad9f19921d822f82", "bytes": 261_701_120 + 3_730_432},
     "prefill": {"sources": ("gqa_attention_learned_gb300/csrc/prefill.cu",
                             "gqa_attention_learned_gb300/csrc/kernels.cuh",
                             "gqa_attention_learned_gb300/csrc/ptx.cuh"),
-                "sha256_16": None, "bytes": None},
+                "sha256_16": "dbe55431d0d26703", "bytes": 220_604_416 + 136_315_392},
 }
 
 
