@@ -195,7 +195,7 @@ __device__ int request_by_size(const DecodeParams &p, int item, int &kv_len) {
 }
 
 template <int NB, bool kVerify>
-__global__ void __launch_bounds__(kNW * 32, kNW <= 8 ? 2 : 1)
+__global__ void __launch_bounds__(kNW * 32, 2)
 decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
               const DecodeParams p) {
   // CTA blockIdx.x: (KV head, head block) unit blockIdx.x % U of (request,
