@@ -210,6 +210,7 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
   const int slot = static_cast<int>(blockIdx.x / units);
   int b = slot / p.num_splits, chunk = slot % p.num_splits;
   int kv_len;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (p.sorted_dispatch) {                 // one chunk per request
     b = request_by_size<kVerify>(p, slot, kv_len);
     chunk = 0;
@@ -217,7 +218,6 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
   } else {
     kv_len = p.kv_lens[b];
   }
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   constexpr int kCols = kHeadsPerTile * NB;       // query rows of this CTA
 
@@ -261,12 +261,22 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
     return j < n_my ? table[first + j * kNW] : -1;
   };
   int ids_cur = load_ids(0), ids_next = load_ids(32);
+  // page ids of this warp's first kStages pages, uniform over the warp
+  int first_ids[kStages];
+#pragma unroll
+  for (int j = 0; j < kStages; ++j) first_ids[j] = __shfl_sync(0xffffffffu, ids_cur, j);
   // This warp's first pages into L2 while the previous kernel on the stream
   // may still be draining (a programmatic launch); the copies below then
   // find them there.
-  if (lane < kStages && ids_cur >= 0 && ids_cur < p.num_pages) {
-    tma_prefetch_l2_3d(&kmap, 0, kvh * kPageSize, ids_cur);
-    tma_prefetch_l2_3d(&vmap, 0, kvh * kPageSize, ids_cur);
+  {
+    int pf = -1;
+#pragma unroll
+    for (int j = 0; j < kStages; ++j)
+      if (lane == j && j < n_my) pf = first_ids[j];
+    if (pf >= 0 && pf < p.num_pages) {
+      tma_prefetch_l2_3d(&kmap, 0, kvh * kPageSize, pf);
+      tma_prefetch_l2_3d(&vmap, 0, kvh * kPageSize, pf);
+    }
   }
 
   // Up to here only kv_lens and page_table were read; everything below may
@@ -330,7 +340,15 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       ids_cur = ids_next;
       ids_next = load_ids(j + 32);
     }
-    const int pid = __shfl_sync(0xffffffffu, ids_cur, j & 31);
+    int pid;
+    if (j < kStages) {                     // the first pages: ids known already
+      pid = first_ids[0];
+#pragma unroll
+      for (int u = 1; u < kStages; ++u)
+        if (j == u) pid = first_ids[u];
+    } else {
+      pid = __shfl_sync(0xffffffffu, ids_cur, j & 31);
+    }
     if (lane == 0) {
       uint64_t *bar = &bars[j % kStages];
       uint8_t *dst = stages + (j % kStages) * kStageBytes;
