@@ -165,11 +165,132 @@ __device__ int request_by_size(const PrefillParams &p, int slot) {
   return -1;                                    // not reached: the classes cover every request
 }
 
-template <bool kPaged, bool kVerify>
+// One 128-key tile of the online softmax for this thread's query row (one
+// row per thread = its tensor-memory lane): NC chunks of 32 scores from S
+// column c0 on (the whole tile: NC = 4, c0 = 0; a key half: NC = 2, c0 = 0 or
+// 64), masks, the reference max m (moved only by more than kRescaleLog2),
+// P = 2^(s scale - m) in bf16 into tensor memory once the previous P V has
+// read it, d updated, O rescaled when m moved.  Returns false when a wait
+// timed out.
+template <int NC>
+__device__ __forceinline__ bool softmax_tile(Bars &bar, uint32_t trow, int j, int c0, int limit,
+                                             bool tree, int draft0, uint64_t vis, float sl2,
+                                             bool pos_scale, uint32_t masked_raw, float &m,
+                                             float &d, uint32_t (&x)[4][32]) {
+    // warp-uniform: the tcgen05.ld/st below are .sync.aligned
+    if (!__all_sync(0xffffffffu, mbar_wait(&bar.s_full, j & 1))) return false;
+    tc_fence_after();
+#pragma unroll
+    for (int c = 0; c < NC; ++c) tmem_ld32(trow + kColS + c0 + 32 * c, x[c]);
+    tmem_ld_wait32(x[0]);
+#pragma unroll
+    for (int c = 1; c < NC; ++c) reg_tie32(x[c]);
+    tc_fence_before();
+    mbar_arrive(&bar.s_free);
+    const int k0 = j * kBN + c0;                 // first key of this thread's columns
+    if (__any_sync(0xffffffffu, k0 + 32 * NC > limit)) {   // only tiles on the causal edge
+#pragma unroll
+      for (int c = 0; c < NC; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          if (k0 + 32 * c + e >= limit) x[c][e] = masked_raw;
+    }
+    if (tree && __any_sync(0xffffffffu, k0 + 32 * NC > draft0)) {   // tiles holding draft keys
+#pragma unroll
+      for (int c = 0; c < NC; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int u = k0 + 32 * c + e - draft0;
+          if (u >= 0 && u < 64 && !((vis >> u) & 1)) x[c][e] = masked_raw;
+        }
+    }
+    float mx;
+    if (pos_scale) {
+      float mc[4];                          // independent chains
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        mc[c] = __uint_as_float(x[c][0]);
+#pragma unroll
+        for (int e = 1; e < 31; e += 2)
+          mc[c] = fmax3(mc[c], __uint_as_float(x[c][e]), __uint_as_float(x[c][e + 1]));
+        mc[c] = fmaxf(mc[c], __uint_as_float(x[c][31]));
+      }
+      mx = (NC == 4 ? fmax3(mc[0], mc[1], fmaxf(mc[2], mc[3])) : fmaxf(mc[0], mc[1])) * sl2;
+    } else {
+      mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < NC; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(x[c][e]) * sl2);
+    }
+    const float m_new = fmaxf(m, mx);
+    float alpha = 1.f;
+    bool rescale = false;
+    if (j == 0) {                        // O holds nothing yet: just re-base d
+      if (m_new != -INFINITY) {
+        d *= ex2(m - m_new);
+        m = m_new;
+      }
+    } else if (m_new > m + kRescaleLog2) {
+      alpha = ex2(m - m_new);
+      d *= alpha;
+      m = m_new;
+      rescale = true;
+    }
+    const float mu = m == -INFINITY ? 0.f : m;
+    const uint64_t scale2 = f2_pack(sl2, sl2), negmu2 = f2_pack(-mu, -mu);
+    uint64_t acc[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      acc[c] = 0;                                   // (+0.f, +0.f)
+      pack_chunk(x[c], scale2, negmu2, acc[c]);     // pairs packed in place
+    }
+    float s0, s1;
+    f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), s0, s1);
+    d += s0 + s1;
+    // the previous tile's P V reads P and accumulates O: wait for it
+    if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(&bar.pv_done, (j - 1) & 1))) return false;
+    tc_fence_after();
+#pragma unroll
+    for (int c = 0; c < NC; ++c)
+      tmem_st16(trow + kColP + c0 / 2 + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&x[c][0]));
+    if (NC == 2 && j == 0) {
+      // a half-tile row: the other half's P columns hold zeros for good
+      uint32_t z[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) z[e] = 0u;
+      tmem_st16(trow + kColP + (32 - c0 / 2), z);
+      tmem_st16(trow + kColP + (32 - c0 / 2) + 16, z);
+    }
+    tmem_st_wait();
+    if (__any_sync(0xffffffffu, rescale)) {
+      // rare: scale this row's O (the previous P V has finished, the next
+      // one is issued only after p_full below)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) tmem_ld32(trow + kColO + 32 * h, x[h]);
+      tmem_ld_wait32(x[0]);
+      reg_tie32(x[1]);
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[h][e] = __float_as_uint(__uint_as_float(x[h][e]) * alpha);
+      tmem_st16(trow + kColO, *reinterpret_cast<uint32_t(*)[16]>(&x[0][0]));
+      tmem_st16(trow + kColO + 16, *reinterpret_cast<uint32_t(*)[16]>(&x[0][16]));
+      tmem_st16(trow + kColO + 32, *reinterpret_cast<uint32_t(*)[16]>(&x[1][0]));
+      tmem_st16(trow + kColO + 48, *reinterpret_cast<uint32_t(*)[16]>(&x[1][16]));
+      tmem_st_wait();
+    }
+    tc_fence_before();
+    mbar_arrive(&bar.p_full);
+  return true;
+}
+
+template <bool kPaged, bool kVerify, bool kHalf = false>
 __global__ void __launch_bounds__(kThreads, 2)
 prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
   static_assert(kPaged || !kVerify, "verification reads the paged cache");
+  static_assert(kVerify || !kHalf, "key halves are a verification tile");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint4 nan4 = make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
 
@@ -240,8 +361,20 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
   const int key_end = shift + i0 + rows_tok;               // keys needed, exclusive (<= kv_len)
   const int n_tiles = cdiv(key_end, kBN);
   const int npages = cdiv(kv_len, kPageSize);
+  // Verification with 33 to 64 query rows (kHalf) splits every key tile in two:
+  // the rows are replicated into the next tensor-memory lanes (half_rows
+  // further on), the warps on the original rows take keys 0..63 of each
+  // tile and those on the replica keys 64..127, each half with its own
+  // online softmax (the sink counted in the first half only); the halves
+  // merge by log-sum-exp at the end.  Each softmax warp then does half the
+  // exponentials of a tile (8-node draft tree, 64 rows: 4797 -> 5140 GB/s).
+  // With 32 rows or fewer, one warp's rows measured faster unsplit (4 draft
+  // tokens: 5467 vs 5349 GB/s).
+  const int half_rows = 32 * cdiv(rows, 32);
+  constexpr bool half_keys = kHalf;           // chosen by the host from q_len * group
   // softmax threads with a query row (verification tiles may be partly empty)
-  const int live_threads = kVerify ? min(kBM, 32 * cdiv(rows, 32)) : kBM;
+  const int live_threads =
+      kVerify ? (half_keys ? 2 * half_rows : min(kBM, 32 * cdiv(rows, 32))) : kBM;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -380,7 +513,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     };
     bool ok = true;                 // Q and the first K tiles are on their way
     int pk = page_of(kKStages);     // ids of the next K tile to load
-    ok = ok && __all_sync(0xffffffffu, mbar_wait(&bar.q_full, 0)) && issue_qk(0);
+    ok = ok && __all_sync(0xffffffffu, mbar_wait(&bar.q_full, 0));
+    if (ok && half_keys) {
+      // replica of the query rows at half_rows (a multiple of 8 rows, so the
+      // 128-byte swizzle pattern of every row is unchanged)
+      const uint4 *src = reinterpret_cast<const uint4 *>(sQ);
+      uint4 *dst = reinterpret_cast<uint4 *>(sQ + half_rows * kHeadDim * 2);
+      for (int e = lane; e < half_rows * (kHeadDim * 2 / 16); e += 32) dst[e] = src[e];
+      fence_proxy_async_smem();
+      __syncwarp();
+    }
+    ok = ok && issue_qk(0);
     for (int j = 0; ok && j + 1 < n_tiles; ++j) {
       // S of tile j has been read: compute S of tile j+1 during this softmax
       if (!__all_sync(0xffffffffu, mbar_wait(&bar.s_free, j & 1))) { ok = false; break; }
@@ -436,9 +579,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     // ------------------------------------------------------------- softmax
     const int r = threadIdx.x;                          // row = TMEM lane
     const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    // the query row this thread computes (a replica lane: the same row as
+    // lane r - half_rows) and the first S column of its keys
+    const int lr = half_keys ? r % half_rows : r;
+    const int c0 = half_keys && r >= half_rows && r < 2 * half_rows ? kBN / 2 : 0;
     // token (within the request) and head of this thread's query row
-    const int i = kVerify ? i0 + r / p.group : i0 + r;
-    const int row_head = kVerify ? kvh * p.group + r % p.group : head;
+    const int i = kVerify ? i0 + lr / p.group : i0 + lr;
+    const int row_head = kVerify ? kvh * p.group + lr % p.group : head;
     const bool tree = kVerify && p.tree_mask != nullptr;
     // keys [0, limit) are candidates (causal); with a draft tree, key
     // draft0 + u is visible only if bit u of the row's mask is set
@@ -446,7 +593,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const int draft0 = shift;
     uint64_t vis = 0;
     if constexpr (kVerify) {
-      if (tree && r < rows) vis = p.tree_mask[static_cast<size_t>(seq) * q_len + i];
+      if (tree && lr < rows) vis = p.tree_mask[static_cast<size_t>(seq) * q_len + i];
     }
     const float sl2 = p.scale_log2;
     const bool pos_scale = sl2 >= 0.f;
@@ -458,111 +605,19 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     // only moves when a row max exceeds it by more than kRescaleLog2, at which
     // point O and d are rescaled; out = O/d and lse = m + log2(d) are exact
     // for any reference, and P stays below 2^kRescaleLog2.
-    float m = p.sinks[row_head] * kLog2e;
-    float d = 1.f;
+    float m = c0 == 0 ? p.sinks[row_head] * kLog2e : -INFINITY;   // the sink: first half only
+    float d = c0 == 0 ? 1.f : 0.f;
     bool ok = true;
     uint32_t x[4][32];
 
     const bool live = warp * 32 < live_threads;         // warp-uniform
     for (int j = 0; live && j < n_tiles; ++j) {
-      // warp-uniform: the tcgen05.ld/st below are .sync.aligned
-      if (!__all_sync(0xffffffffu, mbar_wait(&bar.s_full, j & 1))) { ok = false; break; }
-      tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(trow + kColS + 32 * c, x[c]);
-      tmem_ld_wait32(x[0]);
-      reg_tie32(x[1]);
-      reg_tie32(x[2]);
-      reg_tie32(x[3]);
-      tc_fence_before();
-      mbar_arrive(&bar.s_free);
-      const int k0 = j * kBN;
-      if (__any_sync(0xffffffffu, k0 + kBN > limit)) {   // only tiles on the causal edge
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (k0 + 32 * c + e >= limit) x[c][e] = masked_raw;
+      const bool step = softmax_tile<kHalf ? 2 : 4>(bar, trow, j, c0, limit, tree, draft0, vis, sl2,
+                                                    pos_scale, masked_raw, m, d, x);
+      if (!step) {
+        ok = false;
+        break;
       }
-      if (tree && __any_sync(0xffffffffu, k0 + kBN > draft0)) {   // tiles holding draft keys
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int u = k0 + 32 * c + e - draft0;
-            if (u >= 0 && u < 64 && !((vis >> u) & 1)) x[c][e] = masked_raw;
-          }
-      }
-      float mx;
-      if (pos_scale) {
-        float mc[4];                          // four independent chains
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          mc[c] = __uint_as_float(x[c][0]);
-#pragma unroll
-          for (int e = 1; e < 31; e += 2)
-            mc[c] = fmax3(mc[c], __uint_as_float(x[c][e]), __uint_as_float(x[c][e + 1]));
-          mc[c] = fmaxf(mc[c], __uint_as_float(x[c][31]));
-        }
-        mx = fmax3(mc[0], mc[1], fmaxf(mc[2], mc[3])) * sl2;
-      } else {
-        mx = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(x[c][e]) * sl2);
-      }
-      const float m_new = fmaxf(m, mx);
-      float alpha = 1.f;
-      bool rescale = false;
-      if (j == 0) {                        // O holds nothing yet: just re-base d
-        if (m_new != -INFINITY) {
-          d *= ex2(m - m_new);
-          m = m_new;
-        }
-      } else if (m_new > m + kRescaleLog2) {
-        alpha = ex2(m - m_new);
-        d *= alpha;
-        m = m_new;
-        rescale = true;
-      }
-      const float mu = m == -INFINITY ? 0.f : m;
-      const uint64_t scale2 = f2_pack(sl2, sl2), negmu2 = f2_pack(-mu, -mu);
-      uint64_t acc[4];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        acc[c] = 0;                                   // (+0.f, +0.f)
-        pack_chunk(x[c], scale2, negmu2, acc[c]);     // pairs packed in place
-      }
-      float s0, s1;
-      f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), s0, s1);
-      d += s0 + s1;
-      // the previous tile's P V reads P and accumulates O: wait for it
-      if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(&bar.pv_done, (j - 1) & 1))) { ok = false; break; }
-      tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        tmem_st16(trow + kColP + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&x[c][0]));
-      tmem_st_wait();
-      if (__any_sync(0xffffffffu, rescale)) {
-        // rare: scale this row's O (the previous P V has finished, the next
-        // one is issued only after p_full below)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) tmem_ld32(trow + kColO + 32 * h, x[h]);
-        tmem_ld_wait32(x[0]);
-        reg_tie32(x[1]);
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int e = 0; e < 32; ++e) x[h][e] = __float_as_uint(__uint_as_float(x[h][e]) * alpha);
-        tmem_st16(trow + kColO, *reinterpret_cast<uint32_t(*)[16]>(&x[0][0]));
-        tmem_st16(trow + kColO + 16, *reinterpret_cast<uint32_t(*)[16]>(&x[0][16]));
-        tmem_st16(trow + kColO + 32, *reinterpret_cast<uint32_t(*)[16]>(&x[1][0]));
-        tmem_st16(trow + kColO + 48, *reinterpret_cast<uint32_t(*)[16]>(&x[1][16]));
-        tmem_st_wait();
-      }
-      tc_fence_before();
-      mbar_arrive(&bar.p_full);
     }
     if (!live) {
       // no query rows in this warp: nothing to read
@@ -578,10 +633,34 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       ok = false;
     }
     if (!ok) atomicOr(&bar.bad, 1);
+    // second key half: (O, m, d) to shared memory for the first half's
+    // thread (the K ring is idle: every QK^T has completed)
+    float *half2 = reinterpret_cast<float *>(smem + kOffK);
+    constexpr int kHalfStride = kHeadDim + 4;
+    if (half_keys && c0 != 0 && r < 2 * half_rows && lr < rows) {   // replica lanes only
+      float *h2 = half2 + lr * kHalfStride;
+#pragma unroll
+      for (int c = 0; c < kHeadDim; ++c) h2[c] = __uint_as_float(x[c >> 5][c & 31]);
+      h2[kHeadDim] = m;
+      h2[kHeadDim + 1] = d;
+    }
 
     // outputs are written after the CTA-wide barrier below
     __syncthreads();
     const bool failed = bar.bad != 0;
+    if (half_keys && c0 == 0 && r < rows) {
+      // merge the two key halves by log-sum-exp (either may have seen no key)
+      const float *h2 = half2 + r * kHalfStride;
+      const float m2 = h2[kHeadDim], d2 = h2[kHeadDim + 1];
+      const float mm = fmaxf(m, m2);
+      const float w1 = m == -INFINITY ? 0.f : ex2(m - mm);
+      const float w2 = m2 == -INFINITY ? 0.f : ex2(m2 - mm);
+#pragma unroll
+      for (int c = 0; c < kHeadDim; ++c)
+        x[c >> 5][c & 31] = __float_as_uint(__uint_as_float(x[c >> 5][c & 31]) * w1 + h2[c] * w2);
+      d = d * w1 + d2 * w2;
+      m = mm;
+    }
     if (r < rows) {
       const size_t row = static_cast<size_t>(q_start + i) * p.num_qo_heads + row_head;
       const float inv = d > 0.f ? 1.f / d : 0.f;
@@ -617,16 +696,20 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
 
 }  // namespace
 
-template <bool kPaged, bool kVerify>
+template <bool kPaged, bool kVerify, bool kHalf = false>
 static cudaError_t launch_prefill_variant(const CUtensorMap &qmap, const CUtensorMap &kmap,
                            const CUtensorMap &vmap, const PrefillParams &p, unsigned ctas,
                            cudaStream_t stream, bool programmatic) {
-  cudaError_t err = set_smem_once<prefill_kernel<kPaged, kVerify>>(kSmemBytes);
+  cudaError_t err = set_smem_once<prefill_kernel<kPaged, kVerify, kHalf>>(kSmemBytes);
   if (err != cudaSuccess) return err;
   // verification follows the caller's launch mode; prefill launches plainly
-  return launch_kernel(prefill_kernel<kPaged, kVerify>, ctas, kThreads, kSmemBytes, stream,
+  return launch_kernel(prefill_kernel<kPaged, kVerify, kHalf>, ctas, kThreads, kSmemBytes, stream,
                        kVerify && programmatic, qmap, kmap, vmap, p);
 }
+
+#ifndef SA_VERIFY_HALF_KEYS
+#define SA_VERIFY_HALF_KEYS 1
+#endif
 
 cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap,
                            const CUtensorMap &vmap, const PrefillParams &p, cudaStream_t stream,
@@ -636,7 +719,13 @@ cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap,
                                   (p.verify ? p.num_kv_heads : p.num_qo_heads);
   if (ctas == 0) return cudaSuccess;
   if (ctas > 0x7fffffffull) return cudaErrorInvalidConfiguration;
-  if (p.verify) return launch_prefill_variant<true, true>(qmap, kmap, vmap, p, static_cast<unsigned>(ctas), stream, programmatic);
+  if (p.verify) {
+    // one query tile per KV head when verifying (q_len * group <= 128 rows)
+    const int rows = p.max_q_len * p.group;
+    if (SA_VERIFY_HALF_KEYS && rows > 32 && rows <= 64)
+      return launch_prefill_variant<true, true, true>(qmap, kmap, vmap, p, static_cast<unsigned>(ctas), stream, programmatic);
+    return launch_prefill_variant<true, true>(qmap, kmap, vmap, p, static_cast<unsigned>(ctas), stream, programmatic);
+  }
   if (p.paged) return launch_prefill_variant<true, false>(qmap, kmap, vmap, p, static_cast<unsigned>(ctas), stream, false);
   return launch_prefill_variant<false, false>(qmap, kmap, vmap, p, static_cast<unsigned>(ctas), stream, false);
 }

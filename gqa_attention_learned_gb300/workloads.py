@@ -221,13 +221,17 @@ def random_tree_masks(rng, batch, q_len):
 
 
 def verify_batch(seed=5, batch=64, q_len=4, num_qo_heads=64, num_kv_heads=8, min_len=1,
-                 max_len=4096, tree=False, special_sinks=True):
+                 max_len=4096, tree=False, special_sinks=True, kv_lens_first=()):
     """Verification of q_len draft tokens per request (speculative decoding):
     the drafts are the last q_len keys of each request's paged KV, whose
     length is ~ U{max(min_len, q_len)..max_len}; with `tree`, each request
-    carries a random draft tree's masks, else verification is causal."""
+    carries a random draft tree's masks, else verification is causal.
+    kv_lens_first: lengths that replace the drawn ones of the first requests
+    (the pool is built for the final lengths)."""
     rng = np.random.default_rng(seed)
     kv_lens = rng.integers(max(min_len, q_len), max_len + 1, size=batch)
+    for i, n in enumerate(kv_lens_first):
+        kv_lens[i] = int(n)
     q = _bf16(_normal(rng, (batch, q_len, num_qo_heads, HEAD_DIM)))
     sinks = gpt_oss_sinks(rng, num_qo_heads, 2.0, special_sinks)
     masks = random_tree_masks(rng, batch, q_len) if tree else None

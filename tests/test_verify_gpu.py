@@ -146,6 +146,27 @@ def test_tensor_core_route(q_len, hq, hkv, tree):
     assert_lse_close(lse, rl)
 
 
+@pytest.mark.parametrize("q_len,hq,hkv,tree", [(5, 64, 8, False), (6, 64, 8, True),
+                                               (7, 64, 8, False), (3, 32, 2, False),
+                                               (4, 32, 2, True), (8, 64, 8, False)])
+def test_tensor_core_route_key_halves(q_len, hq, hkv, tree):
+    """33 to 64 query rows per KV head: the rows are replicated into the next
+    tensor-memory lanes and each copy takes one half of every key tile, the
+    halves merged at the end; rows past q_len x group in either half are
+    idle.  Lengths from 0 past the drafts (the second half then sees no key
+    in the first tile) up to several tiles."""
+    b = _tc_batch(q_len, hq, hkv)
+    w = workloads.verify_batch(seed=400 + q_len + hq, batch=b, q_len=q_len, num_qo_heads=hq,
+                               num_kv_heads=hkv, max_len=700, tree=tree,
+                               kv_lens_first=(q_len, q_len + 1, 63, 64, 65, 128, 129))
+    assert 32 < q_len * (hq // hkv) <= 64
+    assert sa.verify_plan(b, q_len, hq, hkv, w["max_kv_len"]) == (1, 0)
+    out, lse = run_verify(w)
+    ro, rl = ref_verify(w)
+    assert_out_close(out, ro)
+    assert_lse_close(lse, rl)
+
+
 def test_tensor_core_route_matches_split_kernel_and_poisons_short_requests():
     q_len, hq, hkv = 8, 64, 8
     b = _tc_batch(q_len, hq, hkv)
