@@ -49,11 +49,11 @@ TRAFFIC = {
     "decode": {"sources": ("gqa_attention_learned_gb300/csrc/decode.cu",
                            "gqa_attention_learned_gb300/csrc/kernels.cuh",
                            "gqa_attention_learned_gb300/csrc/ptx.cuh"),
-               "sha256_16": "ad9f19921d822f82", "bytes": 261_701_120 + 3_730_432},
+               "sha256_16": "940cb271012946d4", "bytes": 261_705_472 + 4_472_320},
     "prefill": {"sources": ("gqa_attention_learned_gb300/csrc/prefill.cu",
                             "gqa_attention_learned_gb300/csrc/kernels.cuh",
                             "gqa_attention_learned_gb300/csrc/ptx.cuh"),
-                "sha256_16": "dbe55431d0d26703", "bytes": 220_604_416 + 136_315_392},
+                "sha256_16": "7b80179d271c2817", "bytes": 220_317_952 + 136_148_992},
 }
 
 
