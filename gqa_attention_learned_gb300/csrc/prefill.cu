@@ -645,7 +645,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       h2[kHeadDim + 1] = d;
     }
 
-    // outputs are written after the CTA-wide barrier below
+    // Outputs are written after the CTA-wide barrier below.  Tensor memory is
+    // read no more: the P V warp frees it meanwhile.
+    tc_fence_before();
     __syncthreads();
     const bool failed = bar.bad != 0;
     if (half_keys && c0 == 0 && r < rows) {
@@ -661,33 +663,44 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       d = d * w1 + d2 * w2;
       m = mm;
     }
-    if (r < rows) {
-      const size_t row = static_cast<size_t>(q_start + i) * p.num_qo_heads + row_head;
-      const float inv = d > 0.f ? 1.f / d : 0.f;
-      uint4 *dst = reinterpret_cast<uint4 *>(p.out + row * kHeadDim);
-      auto o = [&](int c) { return __uint_as_float(x[c >> 5][c & 31]) * inv; };
+    const float inv = d > 0.f ? 1.f / d : 0.f;
+    auto packed = [&](int c) {           // 16-byte chunk c of this row (8 outputs)
+      uint4 w;
+      if (failed) return nan4;
+      auto o = [&](int e) { return __uint_as_float(x[e >> 5][e & 31]) * inv; };
+      w.x = pack_bf16(o(8 * c + 0), o(8 * c + 1));
+      w.y = pack_bf16(o(8 * c + 2), o(8 * c + 3));
+      w.z = pack_bf16(o(8 * c + 4), o(8 * c + 5));
+      w.w = pack_bf16(o(8 * c + 6), o(8 * c + 7));
+      return w;
+    };
+    const size_t row = static_cast<size_t>(q_start + i) * p.num_qo_heads + row_head;
+    if (!kVerify && r - lane + 32 <= rows && !failed) {
+      // Full 32-row slices of prefill / extend: each warp puts its rows in the
+      // query buffer (free since the last QK^T completed) and reads them back
+      // so that 8 lanes cover one row's 128 contiguous bytes: every store
+      // writes 4 whole rows instead of a 16-byte piece of 32 rows 8 KB apart.
+      uint4 *sw = reinterpret_cast<uint4 *>(sQ) + (r - lane) * 8;     // this warp's 32 rows
 #pragma unroll
-      for (int c = 0; c < kHeadDim / 8; ++c) {
-        uint4 w;
-        if (failed) {
-          w = nan4;
-        } else {
-          w.x = pack_bf16(o(8 * c + 0), o(8 * c + 1));
-          w.y = pack_bf16(o(8 * c + 2), o(8 * c + 3));
-          w.z = pack_bf16(o(8 * c + 4), o(8 * c + 5));
-          w.w = pack_bf16(o(8 * c + 6), o(8 * c + 7));
-        }
-        dst[c] = w;
+      for (int c = 0; c < kHeadDim / 8; ++c) sw[lane * 8 + (c ^ (lane & 7))] = packed(c);
+      __syncwarp();
+      const int cc = lane & 7;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int rr = 4 * k + (lane >> 3);                  // row within the warp's slice
+        const size_t grow = static_cast<size_t>(q_start + i0 + (r - lane) + rr) * p.num_qo_heads + head;
+        reinterpret_cast<uint4 *>(p.out + grow * kHeadDim)[cc] = sw[rr * 8 + (cc ^ (rr & 7))];
       }
-      if (p.lse) p.lse[row] = failed ? NAN : (d > 0.f ? (m + lg2(d)) * kLn2 : -INFINITY);
+    } else if (r < rows) {
+      uint4 *dst = reinterpret_cast<uint4 *>(p.out + row * kHeadDim);
+#pragma unroll
+      for (int c = 0; c < kHeadDim / 8; ++c) dst[c] = packed(c);
     }
-    tc_fence_before();
-    __syncthreads();
+    if (r < rows && p.lse) p.lse[row] = failed ? NAN : (d > 0.f ? (m + lg2(d)) * kLn2 : -INFINITY);
     return;
   }
-  __syncthreads();          // matches the softmax warps' output barrier
   tc_fence_before();
-  __syncthreads();          // everybody is done with tensor memory
+  __syncthreads();          // the softmax warps have read O: tensor memory is free
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
