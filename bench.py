@@ -14,8 +14,9 @@ prefill in TFLOP/s, the mixed serving batch) and the float64 CPU oracle.
 Inputs are synthetic, seeded and resident in HBM before timing (``value``);
 ``e2e`` repeats the decode through the public API with pinned host buffers
 and the per-step copies inside the timed region (uploads and downloads on
-their own streams, double-buffered, as a serving loop overlaps them).  Two copies of the KV pool
-alternate between steps, so no step finds the previous step's KV in L2.
+their own streams, double-buffered, as a serving loop overlaps them).  Copies of each KV pool
+are cycled one per step, like the pools of consecutive layers, so that a page comes back only
+after 4 GB of other pages: no step finds an earlier step's KV in L2.
 Under torchrun each rank runs its own seeded batch (weak scaling, no
 collective on the data path); rank 0 prints the max-over-ranks time.
 """
@@ -49,11 +50,11 @@ TRAFFIC = {
     "decode": {"sources": ("gqa_attention_learned_gb300/csrc/decode.cu",
                            "gqa_attention_learned_gb300/csrc/kernels.cuh",
                            "gqa_attention_learned_gb300/csrc/ptx.cuh"),
-               "sha256_16": "940cb271012946d4", "bytes": 261_705_472 + 4_472_320},
+               "sha256_16": "6bd6fa4ecfea8712", "bytes": 261_729_536 + 3_153_920},
     "prefill": {"sources": ("gqa_attention_learned_gb300/csrc/prefill.cu",
                             "gqa_attention_learned_gb300/csrc/kernels.cuh",
                             "gqa_attention_learned_gb300/csrc/ptx.cuh"),
-                "sha256_16": "7b80179d271c2817", "bytes": 220_317_952 + 136_148_992},
+                "sha256_16": "f39f01e674f405cb", "bytes": 223_187_200 + 139_803_904},
 }
 
 
@@ -251,6 +252,27 @@ def _time_steps(torch, fn, steps, warmup, stream):
     return start.elapsed_time(end) / 1e3
 
 
+# Bytes of other pages read before a page comes back (about 30x L2).
+REUSE_BYTES = 4e9
+
+
+def kv_pools(torch, k, v, dev):
+    """Copies of a KV pool on `dev`, cycled one per step like the pools of
+    consecutive layers: a page is read again only after REUSE_BYTES of other
+    pages, so no step finds pages of an earlier one in L2, whatever eviction
+    priority the kernels give their loads."""
+    import math
+    pool_bytes = 2 * k.numel() * k.element_size()
+    n = min(32, max(2, math.ceil(REUSE_BYTES / pool_bytes) + 1))
+    first = (k.to(dev), v.to(dev))
+    return [first] + [(first[0].clone(), first[1].clone()) for _ in range(n - 1)]
+
+
+def pools_label(pools):
+    mb = 2 * pools[0][0].numel() * pools[0][0].element_size() / 1e6
+    return f"{len(pools)} KV pool copies ({len(pools)} x {mb:.0f} MB) cycled, one per step"
+
+
 def run_decode_arm(args, rank, dev):
     import torch
 
@@ -262,8 +284,7 @@ def run_decode_arm(args, rank, dev):
     lens = [int(x) for x in w["kv_lens"]]
     nbytes = decode_bytes(lens, hq, hkv)
     q = w["q"].to(dev)
-    pools = [(w["k_cache"].to(dev), w["v_cache"].to(dev))]
-    pools.append((pools[0][0].clone(), pools[0][1].clone()))
+    pools = kv_pools(torch, w["k_cache"], w["v_cache"], dev)
     table, kv_lens, sinks = w["page_table"].to(dev), w["kv_lens"].to(dev), w["sinks"].to(dev)
     max_kv = w["max_kv_len"]
     splits, ws_bytes = sa.decode_plan(64, hq, hkv, max_kv, args.splits)
@@ -273,7 +294,7 @@ def run_decode_arm(args, rank, dev):
     stream = torch.cuda.current_stream()
 
     def step(i, mode=None):
-        kc, vc = pools[i & 1]
+        kc, vc = pools[i % len(pools)]
         sa.decode(q, kc, vc, table, kv_lens, sinks, w["scale"], max_kv, out=out, lse=lse,
                   num_splits=args.splits, workspace=ws, stream=stream, programmatic=mode)
 
@@ -318,7 +339,7 @@ def run_decode_arm(args, rank, dev):
 
     def e2e_step(i):
         in_d.copy_(in_h, non_blocking=True)
-        kc, vc = pools[i & 1]
+        kc, vc = pools[i % len(pools)]
         sa.decode(q_e, kc, vc, table_e, lens_e, sinks, w["scale"], max_kv, out=out_e, lse=lse_e,
                   num_splits=args.splits, workspace=ws, stream=stream)
         out_h.copy_(out_d, non_blocking=True)
@@ -352,7 +373,7 @@ def run_decode_arm(args, rank, dev):
             cs.wait_event(b["up"])
             if i >= 2:
                 cs.wait_event(b["down"])            # download i-2 has read this output set
-            kc, vc = pools[i & 1]
+            kc, vc = pools[i % len(pools)]
             q_b, table_b, lens_b = b["ins"]
             out_b, lse_b = b["outs"]
             sa.decode(q_b, kc, vc, table_b, lens_b, sinks, w["scale"], max_kv, out=out_b,
@@ -410,7 +431,7 @@ def run_decode_arm(args, rank, dev):
     kv_pool_bytes = 2 * k_h.numel() * k_h.element_size()
 
     def e2e_kv_step(i):
-        kc, vc = pools[i & 1]
+        kc, vc = pools[i % len(pools)]
         kc.copy_(k_h, non_blocking=True)
         vc.copy_(v_h, non_blocking=True)
         e2e_step(i)
@@ -419,9 +440,9 @@ def run_decode_arm(args, rank, dev):
     kv_secs = _time_steps(torch, e2e_kv_step, kv_steps, 2, stream)
     _, _, kv_gbps = aggregate(nbytes * kv_steps, kv_secs, dev)
 
-    pool_mb = pools[0][0].numel() * pools[0][0].element_size() * 2 / 1e6
+    pool_label = pools_label(pools)
     return dict(w=w, nbytes=nbytes, secs=t_max, gbps=gbps / 1e9, splits=splits,
-                plain_gbps=plain_gbps / 1e9, plain_steps=plain_steps, pool_mb=pool_mb,
+                plain_gbps=plain_gbps / 1e9, plain_steps=plain_steps, pool_label=pool_label,
                 launches_per_step=launches_per_step, clocks=clocks.summary(),
                 e2e=dict(value=e2e_gbps / 1e9, unit="GB/s", h2d_bytes_per_step=h2d,
                          d2h_bytes_per_step=d2h, steps=e2e_steps,
@@ -456,8 +477,7 @@ def run_graph_decode(args, rank, dev, peaks):
     lens = [int(x) for x in w["kv_lens"]]
     nbytes = decode_bytes(lens, hq, hkv)
     q = w["q"].to(dev)
-    pools = [(w["k_cache"].to(dev), w["v_cache"].to(dev))]
-    pools.append((pools[0][0].clone(), pools[0][1].clone()))
+    pools = kv_pools(torch, w["k_cache"], w["v_cache"], dev)
     table, kv_lens, sinks = w["page_table"].to(dev), w["kv_lens"].to(dev), w["sinks"].to(dev)
     max_kv = w["max_kv_len"]
     _, ws_bytes = sa.decode_plan(64, hq, hkv, max_kv)
@@ -466,7 +486,7 @@ def run_graph_decode(args, rank, dev, peaks):
     lse = torch.empty(q.shape[0], hq, dtype=torch.float32, device=dev)
 
     def call(i):
-        kc, vc = pools[i & 1]
+        kc, vc = pools[i % len(pools)]
         sa.decode(q, kc, vc, table, kv_lens, sinks, w["scale"], max_kv, out=out, lse=lse,
                   workspace=ws)
 
@@ -477,11 +497,11 @@ def run_graph_decode(args, rank, dev, peaks):
         call(1)
     torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
-    # one graph per step, and one graph holding 10 steps (the two pool copies
-    # alternating), whose launches keep their programmatic edges
-    per_graph = 10
+    # one graph per step (per pool copy), and one graph holding a step on
+    # every pool copy, whose launches keep their programmatic edges
+    per_graph = len(pools)
     graphs = []
-    for i in range(2):
+    for i in range(len(pools)):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             call(i)
@@ -493,7 +513,7 @@ def run_graph_decode(args, rank, dev, peaks):
     stream = torch.cuda.current_stream()
 
     def step(i):
-        graphs[i & 1].replay()
+        graphs[i % len(graphs)].replay()
 
     steps = max(100, args.steps // 2)
     secs = _time_steps(torch, step, steps, args.warmup, stream)
@@ -506,14 +526,14 @@ def run_graph_decode(args, rank, dev, peaks):
     return dict(workload=DECODE_WORKLOAD + " (CUDA graph replay)", steps=steps,
                 ms_per_step=1e3 * t / steps, value=round(bps / 1e9, 2), unit="GB/s",
                 frac_of_hbm=round(bps / 1e9 / peaks["hbm_gbs"], 4),
-                ten_step_graph=dict(steps=reps * per_graph,
+                multi_step_graph=dict(steps=reps * per_graph, steps_per_graph=per_graph,
                                     ms_per_step=1e3 * t10 / (reps * per_graph),
                                     value=round(bps10 / 1e9, 2), unit="GB/s",
                                     frac_of_hbm=round(bps10 / 1e9 / peaks["hbm_gbs"], 4)),
                 note="plan from host-side sizes; chunks per request derived on the device from "
                      "kv_lens, so the captured launch serves new lengths and page tables; value: "
                      "one graph per step (no programmatic edge between graph launches); "
-                     "ten_step_graph: 10 steps per graph")
+                     "multi_step_graph: one graph holding a step on every pool copy")
 
 
 def run_long_decode(args, rank, dev):
@@ -526,27 +546,30 @@ def run_long_decode(args, rank, dev):
     hq, hkv = w["num_qo_heads"], w["num_kv_heads"]
     lens = [int(x) for x in w["kv_lens"]]
     nbytes = decode_bytes(lens, hq, hkv)
-    args_d = [w[n].to(dev) for n in ("q", "k_cache", "v_cache", "page_table", "kv_lens", "sinks")]
+    q, table, kv_lens, sinks = (w[n].to(dev) for n in ("q", "page_table", "kv_lens", "sinks"))
+    pools = kv_pools(torch, w["k_cache"], w["v_cache"], dev)
     res = {}
     for label, splits in (("auto", 0), ("8 splits", 8)):
         s, ws_bytes = sa.decode_plan(len(lens), hq, hkv, w["max_kv_len"], splits)
         ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
-        out = torch.empty_like(args_d[0])
+        out = torch.empty_like(q)
         lse = torch.empty(len(lens), hq, dtype=torch.float32, device=dev)
         stream = torch.cuda.current_stream()
 
         def step(i, splits=splits, ws=ws, out=out, lse=lse):
-            sa.decode(*args_d, w["scale"], w["max_kv_len"], out=out, lse=lse, num_splits=splits,
-                      workspace=ws, stream=stream)
+            kc, vc = pools[i % len(pools)]
+            sa.decode(q, kc, vc, table, kv_lens, sinks, w["scale"], w["max_kv_len"], out=out,
+                      lse=lse, num_splits=splits, workspace=ws, stream=stream)
 
         steps = max(20, args.steps // 50)
         secs = _time_steps(torch, step, steps, args.warmup, stream)
         _, t, gbps = aggregate(nbytes * steps, secs, dev)
         res[label] = dict(splits=s, ms_per_step=1e3 * t / steps, value=gbps / 1e9, unit="GB/s")
-    del args_d
+    label = pools_label(pools)
+    del pools
     torch.cuda.empty_cache()
     return dict(workload="long-context split-KV decode: 64 q / 8 KV heads, batch 8, "
-                         "kv_len U[32768,131072], bf16 paged KV (page 16)",
+                         "kv_len U[32768,131072], bf16 paged KV (page 16); " + label,
                 kv_bytes=nbytes, runs=res)
 
 
@@ -564,8 +587,7 @@ def run_verify(args, rank, dev, peaks):
         lens = [int(x) for x in w["kv_lens"]]
         nbytes = verify_bytes(lens, q_len, hq, hkv, tree)
         q = w["q"].to(dev)
-        pools = [(w["k_cache"].to(dev), w["v_cache"].to(dev))]
-        pools.append((pools[0][0].clone(), pools[0][1].clone()))
+        pools = kv_pools(torch, w["k_cache"], w["v_cache"], dev)
         table, kv_lens, sinks = w["page_table"].to(dev), w["kv_lens"].to(dev), w["sinks"].to(dev)
         mask = None if w["tree_mask"] is None else w["tree_mask"].to(dev)
         splits, ws_bytes = sa.verify_plan(len(lens), q_len, hq, hkv, w["max_kv_len"])
@@ -576,7 +598,7 @@ def run_verify(args, rank, dev, peaks):
 
         def step(i, q=q, pools=pools, table=table, kv_lens=kv_lens, sinks=sinks, mask=mask,
                  w=w, out=out, lse=lse, ws=ws):
-            kc, vc = pools[i & 1]
+            kc, vc = pools[i % len(pools)]
             sa.verify(q, kc, vc, table, kv_lens, sinks, w["scale"], w["max_kv_len"],
                       tree_mask=mask, out=out, lse=lse, workspace=ws, stream=stream)
 
@@ -590,8 +612,8 @@ def run_verify(args, rank, dev, peaks):
         del pools, q
         torch.cuda.empty_cache()
     return dict(workload="draft-token verification on the gpt-oss-20b decode batch: 64 requests, "
-                         "kv_len U[q_len,4096], 64 q / 8 KV heads, bf16 paged KV; two KV pool "
-                         "copies alternate (inputs larger than L2)",
+                         "kv_len U[q_len,4096], 64 q / 8 KV heads, bf16 paged KV; copies of the KV "
+                         "pool cycled one per step (a page re-read after 4 GB of others)",
                 runs=res)
 
 
@@ -715,7 +737,8 @@ def run_mixed(args, rank, dev, peaks):
     m = workloads.mixed_batch(seed=4 + 1000 * rank)
     d, e = m["decode"], m["extend"]
     hq, hkv = m["num_qo_heads"], m["num_kv_heads"]
-    kc, vc, sinks = m["k_cache"].to(dev), m["v_cache"].to(dev), m["sinks"].to(dev)
+    pools = kv_pools(torch, m["k_cache"], m["v_cache"], dev)
+    sinks = m["sinks"].to(dev)
     dq, dt, dl = d["q"].to(dev), d["page_table"].to(dev), d["kv_lens"].to(dev)
     eq, ecu, et, el = (e["q"].to(dev), e["cu_seqlens_q"].to(dev), e["page_table"].to(dev),
                        e["kv_lens"].to(dev))
@@ -735,6 +758,7 @@ def run_mixed(args, rank, dev, peaks):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
 
     def step(i, record=False):
+        kc, vc = pools[i % len(pools)]
         if record:
             ev[i][0].record(stream)
         sa.decode(dq, kc, vc, dt, dl, sinks, m["scale"], d["max_kv_len"], out=dout, lse=dlse,
@@ -762,7 +786,7 @@ def run_mixed(args, rank, dev, peaks):
     ideal = nbytes / (peaks["hbm_gbs"] * 1e9) + flops / (peaks["bf16_tflops"] * 1e12)
     return dict(workload="mixed serving batch: 32 decode requests (kv_len U[512,16384]) + 4 "
                          "chunked-prefill requests of 2048 tokens on prefixes U[0,14336], one "
-                         "shuffled page pool, two launches on one stream",
+                         "shuffled page pool, two launches on one stream; " + pools_label(pools),
                 steps=steps, ms_per_step=1e3 * t_all / steps,
                 decode={"value": round(dec_gbs, 2), "unit": "GB/s", "bytes": nbytes,
                         "ms": 1e3 * t_dec / steps},
@@ -787,8 +811,7 @@ def run_gqa(args, rank, dev, peaks):
                                    num_kv_heads=hkv)
         nbytes = decode_bytes([int(x) for x in w["kv_lens"]], hq, hkv)
         q = w["q"].to(dev)
-        pools = [(w["k_cache"].to(dev), w["v_cache"].to(dev))]
-        pools.append((pools[0][0].clone(), pools[0][1].clone()))
+        pools = kv_pools(torch, w["k_cache"], w["v_cache"], dev)
         table, lens, sinks = w["page_table"].to(dev), w["kv_lens"].to(dev), w["sinks"].to(dev)
         splits, ws_bytes = sa.decode_plan(b, hq, hkv, w["max_kv_len"])
         ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
@@ -797,7 +820,7 @@ def run_gqa(args, rank, dev, peaks):
         for mode in (True, False):
             def step(i, mode=mode, q=q, pools=pools, table=table, lens=lens, sinks=sinks, w=w,
                      ws=ws):
-                kc, vc = pools[i & 1]
+                kc, vc = pools[i % len(pools)]
                 sa.decode(q, kc, vc, table, lens, sinks, w["scale"], w["max_kv_len"],
                           workspace=ws, stream=stream, programmatic=mode)
             steps = max(50, args.steps // 20)
@@ -809,8 +832,8 @@ def run_gqa(args, rank, dev, peaks):
         res[f"{hq} q / {hkv} kv heads, {b} requests"] = run
         del pools, q
         torch.cuda.empty_cache()
-    return dict(workload="decode, kv_len U[1,4096], bf16 paged KV (page 16, shuffled), two KV "
-                         "pool copies alternate", runs=res)
+    return dict(workload="decode, kv_len U[1,4096], bf16 paged KV (page 16, shuffled), copies of "
+                         "the KV pool cycled one per step", runs=res)
 
 
 SECTIONS = {"long": "long_decode", "graph": "graph_decode", "verify": "verify",
@@ -857,7 +880,7 @@ def section_summary(extra, peaks):
     if "graph_decode" in extra:
         g = extra["graph_decode"]
         out.update(graph_decode_frac=g["frac_of_hbm"],
-                   graph10_decode_frac=g["ten_step_graph"]["frac_of_hbm"])
+                   graph_multi_step_decode_frac=g["multi_step_graph"]["frac_of_hbm"])
     if "verify" in extra:
         for key, label in (("verify_mtp2", "mtp 2 tokens"), ("verify_4tok", "4 tokens causal"),
                            ("verify_tree8", "8-node tree")):
@@ -933,8 +956,7 @@ def gpu_arm(args):
                    "kv_tokens": sum(int(x) for x in d["w"]["kv_lens"]),
                    "num_splits": d["splits"],
                    "launch": "plain" if args.plain_launch else "programmatic dependent launch",
-                   "l2": f"inputs larger than L2: two KV pool copies "
-                         f"(2 x {d['pool_mb']:.0f} MB) alternate"},
+                   "l2": "inputs larger than L2: " + d["pool_label"]},
         "roofline": roofline,
         "e2e": {k: v for k, v in d["e2e"].items() if k != "note"},
         "gpu_launches": args.steps * d["launches_per_step"],

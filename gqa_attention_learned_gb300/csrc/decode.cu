@@ -334,6 +334,12 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
     for (int i = 0; i < 4; ++i) o[nb][i][0] = o[nb][i][1] = o[nb][i][2] = o[nb][i][3] = 0.f;
 
   bool lane_bad = false;     // meaningful on lane 0
+  // With one CTA per (request, KV head, chunk) every page is read once: its
+  // lines go first when L2 needs room, so the small tensors every launch
+  // re-reads (kv_lens, page table, q) and the outputs stay.  Wider GQA groups
+  // split into head blocks read each page twice, the second time from L2.
+  const bool read_once = p.head_blocks == 1;
+  const uint64_t evict_first = l2_policy_evict_first();
 
   auto issue = [&](int j) {  // all lanes call; lane 0 issues
     if ((j & 31) == 0 && j > 0) {
@@ -355,8 +361,13 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       if (pid >= 0 && pid < p.num_pages) {
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(bar, kStageBytes);
-        tma_load_3d(dst, &kmap, bar, 0, kvh * kPageSize, pid);
-        tma_load_3d(dst + kTileBytes, &vmap, bar, 0, kvh * kPageSize, pid);
+        if (read_once) {
+          tma_load_3d_hint(dst, &kmap, bar, 0, kvh * kPageSize, pid, evict_first);
+          tma_load_3d_hint(dst + kTileBytes, &vmap, bar, 0, kvh * kPageSize, pid, evict_first);
+        } else {
+          tma_load_3d(dst, &kmap, bar, 0, kvh * kPageSize, pid);
+          tma_load_3d(dst + kTileBytes, &vmap, bar, 0, kvh * kPageSize, pid);
+        }
       } else {
         lane_bad = true;     // skip the copy; the phase still completes
         mbar_arrive(bar);

@@ -421,7 +421,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       const unsigned mask = __ballot_sync(0xffffffffu, ok);
       if (lane == 0) mbar_arrive_expect_tx(full, __popc(mask) * kPageSize * kHeadDim * 2);
       __syncwarp();
-      if (ok) tma_load_3d(dst + lane * kPageSize * kHeadDim * 2, map, full, 0, kvh * kPageSize, pid);
+      if (ok) {
+        if (kVerify && p.num_q_tiles == 1)    // the only reader of these pages
+          tma_load_3d_hint(dst + lane * kPageSize * kHeadDim * 2, map, full, 0, kvh * kPageSize,
+                           pid, l2_policy_evict_first());
+        else
+          tma_load_3d(dst + lane * kPageSize * kHeadDim * 2, map, full, 0, kvh * kPageSize, pid);
+      }
     } else {
       if (lane == 0) {
         mbar_arrive_expect_tx(full, kTileBytes);
