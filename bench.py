@@ -861,8 +861,67 @@ def run_gqa(args, rank, dev, peaks):
                          "the KV pool cycled one per step", runs=res)
 
 
+def run_layer(args, rank, dev, peaks):
+    """The attention of a decode layer as a model runs it: per step the
+    prologue of the step's 64 new tokens (QKV bias, YaRN rotation of q and k,
+    k and v written into each request's newest cache slot), then the decode
+    over the cache that now holds them, each step on its own pool copy.  With
+    programmatic launch the decode ranks its requests and reads its page ids
+    while the prologue runs; the same steps with plain launches beside."""
+    import torch
+
+    import gqa_attention_learned_gb300 as sa
+    from gqa_attention_learned_gb300 import workloads
+
+    w = workloads.decode_batch(seed=1 + 1000 * rank)
+    hq, hkv = w["num_qo_heads"], w["num_kv_heads"]
+    lens = [int(x) for x in w["kv_lens"]]
+    b = len(lens)
+    table_h = w["page_table"]
+    pools = kv_pools(torch, w["k_cache"], w["v_cache"], dev)
+    table, kv_lens, sinks = table_h.to(dev), w["kv_lens"].to(dev), w["sinks"].to(dev)
+    # request r's newest token: position kv_len - 1 and its cache slot
+    pos = torch.tensor([max(n - 1, 0) for n in lens], dtype=torch.int32, device=dev)
+    slots = torch.tensor([int(table_h[r, (n - 1) // 16]) * 16 + (n - 1) % 16 if n > 0 else -1
+                          for r, n in enumerate(lens)], dtype=torch.int32, device=dev)
+    gen = torch.Generator().manual_seed(11 + 1000 * rank)
+    width = (hq + 2 * hkv) * HEAD_DIM
+    qkv = torch.randn(b, width, generator=gen).to(torch.bfloat16).to(dev)
+    bias = (0.5 * torch.randn(width, generator=gen)).to(torch.bfloat16).to(dev)
+    inv, msc = sa.yarn_table()
+    q_new = torch.empty(b, hq, HEAD_DIM, dtype=torch.bfloat16, device=dev)
+    out = torch.empty_like(q_new)
+    lse = torch.empty(b, hq, dtype=torch.float32, device=dev)
+    _, ws_bytes = sa.decode_plan(b, hq, hkv, w["max_kv_len"])
+    ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    nbytes = prologue_bytes(b, hq, hkv) + decode_bytes(lens, hq, hkv)
+    res = {}
+    for mode in (True, False):
+        def step(i, mode=mode):
+            kc, vc = pools[i % len(pools)]
+            sa.qkv_prologue(qkv, bias, pos, slots, inv, msc, kc, vc, hq, hkv, q_out=q_new,
+                            stream=stream)
+            sa.decode(q_new, kc, vc, table, kv_lens, sinks, w["scale"], w["max_kv_len"], out=out,
+                      lse=lse, workspace=ws, stream=stream, programmatic=mode)
+
+        steps = max(200, args.steps // 10)
+        secs = _time_steps(torch, step, steps, args.warmup, stream)
+        _, t, bps = aggregate(nbytes * steps, secs, dev)
+        res["programmatic" if mode else "plain"] = dict(
+            us_per_step=round(1e6 * t / steps, 2), value=round(bps / 1e9, 2), unit="GB/s",
+            frac_of_hbm=round(bps / 1e9 / peaks["hbm_gbs"], 4))
+    label = pools_label(pools)
+    del pools
+    torch.cuda.empty_cache()
+    return dict(workload="decode layer: prologue of 64 new tokens (bias, YaRN q/k, paged k/v write) "
+                         "then decode of the gpt-oss-20b batch, two launches per step; " + label,
+                bytes_per_step=nbytes, launches_per_step=2, runs=res)
+
+
 SECTIONS = {"long": "long_decode", "graph": "graph_decode", "verify": "verify",
-            "prologue": "prologue", "prefill": "prefill", "mixed": "mixed", "gqa": "gqa"}
+            "prologue": "prologue", "prefill": "prefill", "mixed": "mixed", "gqa": "gqa",
+            "layer": "layer"}
 
 
 def only_section(args):
@@ -884,7 +943,8 @@ def only_section(args):
           "prologue": lambda: run_prologue(args, rank, dev, peaks),
           "prefill": lambda: run_prefill(args, rank, dev, peaks),
           "mixed": lambda: run_mixed(args, rank, dev, peaks),
-          "gqa": lambda: run_gqa(args, rank, dev, peaks)}[args.only]
+          "gqa": lambda: run_gqa(args, rank, dev, peaks),
+          "layer": lambda: run_layer(args, rank, dev, peaks)}[args.only]
     out = fn()
     if rank == 0:
         print(json.dumps({"section": SECTIONS[args.only], **out}), flush=True)
@@ -928,6 +988,11 @@ def section_summary(extra, peaks):
         r = extra["prologue"]["runs"].get("prefill 4 sequences")
         if r:
             out.update(prologue_prefill_frac=r["frac_of_hbm"])
+    if "layer" in extra:
+        r = extra["layer"]["runs"]
+        out.update(layer_frac=r["programmatic"]["frac_of_hbm"],
+                   layer_us_per_step=r["programmatic"]["us_per_step"],
+                   layer_plain_frac=r["plain"]["frac_of_hbm"])
     return out
 
 
@@ -963,6 +1028,8 @@ def gpu_arm(args):
             extra["mixed"] = run_mixed(args, rank, dev, peaks)
         if "gqa" in sections:
             extra["gqa"] = run_gqa(args, rank, dev, peaks)
+        if "layer" in sections:
+            extra["layer"] = run_layer(args, rank, dev, peaks)
     roofline = {"bound": "hbm", "achieved": round(kernel_gbps, 2), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(kernel_gbps / peaks["hbm_gbs"], 4),
                 "traffic": kernel_traffic("decode"), "peak_source": peak_src,
@@ -1115,7 +1182,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--splits", type=int, default=0, help="decode split count (0 = planned)")
     ap.add_argument("--quick", action="store_true", help="headline decode only")
-    ap.add_argument("--sections", default="graph,long,verify,prologue,prefill,mixed",
+    ap.add_argument("--sections", default="graph,long,verify,prologue,prefill,mixed,layer",
                     help="extra sections after the headline decode")
     ap.add_argument("--plain-launch", action="store_true",
                     help="launch decode kernels without programmatic dependent launch")

@@ -51,6 +51,10 @@ prologue_kernel(const __grid_constant__ PrologueParams p) {
   // request ranking now; it waits for this grid to finish before reading q
   // or the caches.
   launch_dependents();
+  // This kernel is itself launched programmatically: it reads and writes
+  // nothing before the previous kernel on the stream has finished, so only
+  // its launch and set-up overlap that kernel's last CTAs.
+  grid_dependency_wait();
   const int tok0 = blockIdx.x * kTok;
   for (int j = threadIdx.x; j < kTok * kPairs; j += kThreads) {
     const int tt = j / kPairs, i = j % kPairs;
@@ -134,12 +138,11 @@ prologue_kernel(const __grid_constant__ PrologueParams p) {
 
 cudaError_t launch_prologue(const PrologueParams &p, cudaStream_t stream) {
   if (p.num_tokens <= 0) return cudaSuccess;
-  if (p.num_tokens <= 4096) {        // small batches: one token per CTA, more SMs busy
-    prologue_kernel<1><<<static_cast<unsigned>(p.num_tokens), kThreads, 0, stream>>>(p);
-  } else {
-    prologue_kernel<4><<<static_cast<unsigned>((p.num_tokens + 3) / 4), kThreads, 0, stream>>>(p);
-  }
-  return cudaGetLastError();
+  if (p.num_tokens <= 4096)          // small batches: one token per CTA, more SMs busy
+    return launch_kernel(prologue_kernel<1>, static_cast<unsigned>(p.num_tokens), kThreads, 0,
+                         stream, true, p);
+  return launch_kernel(prologue_kernel<4>, static_cast<unsigned>((p.num_tokens + 3) / 4), kThreads,
+                       0, stream, true, p);
 }
 
 }  // namespace sa

@@ -332,6 +332,11 @@ SINKATTN_API int sinkattn_yarn_table(int head_dim, double base, double factor,
  *   q_out        : bf16 [num_tokens][num_qo_heads][head_dim]
  *   k_cache, v_cache : the paged cache (see conventions), num_pages pages
  * Two tokens mapped to the same slot race (one of them wins).
+ * Launch: always programmatic, whatever the default above.  The kernel reads
+ * and writes nothing before the kernel launched before it on the stream has
+ * finished (so it puts no contract on the caller); only its launch and set-up
+ * overlap that kernel's last CTAs.  It lets a programmatically launched decode
+ * or verification after it be scheduled at once.
  */
 #define SINKATTN_ROPE_HALF 0
 #define SINKATTN_ROPE_INTERLEAVED 1

@@ -124,3 +124,48 @@ def test_prologue_then_decode():
                            sinks.numpy().astype(np.float64), 0.125)
     assert_out_close(out.cpu(), ro)
     assert_lse_close(lse.cpu(), rl)
+
+
+def test_prologue_waits_for_the_decode_before_it():
+    """decode -> prologue -> decode on one stream, all launched
+    programmatically, the prologue writing its q into the buffer the first
+    decode reads and its k / v into the pages both decodes read.  600
+    requests give the first decode several waves of CTAs, so a prologue that
+    wrote before that decode finished would change its later CTAs' q."""
+    hq, hkv = 64, 8
+    rng = np.random.default_rng(21)
+    starts = [int(x) for x in rng.integers(1, 900, size=600)]
+    w = workloads.prologue_batch([1] * len(starts), starts, seed=22)
+    sinks = workloads.gpt_oss_sinks(rng, hq)
+    q1 = torch.from_numpy(rng.standard_normal((len(starts), hq, 64)).astype(np.float32)).to(torch.bfloat16)
+    inv, ms = sa.yarn_table()
+    kc, vc = w["k_cache"].to(DEV), w["v_cache"].to(DEV)
+    table, sk = w["page_table"].to(DEV), sinks.to(DEV)
+    lens1 = torch.tensor(starts, dtype=torch.int32)
+    lens2 = lens1 + 1
+    qbuf = q1.to(DEV)
+    out1, lse1 = sa.decode(qbuf, kc, vc, table, lens1.to(DEV), sk, 0.125, int(lens2.max()),
+                           programmatic=True)
+    sa.qkv_prologue(w["qkv"].to(DEV), w["bias"].to(DEV), w["positions"].to(DEV),
+                    w["slot_mapping"].to(DEV), inv, ms, kc, vc, hq, hkv, q_out=qbuf)
+    out2, lse2 = sa.decode(qbuf, kc, vc, table, lens2.to(DEV), sk, 0.125, int(lens2.max()),
+                           programmatic=True)
+    torch.cuda.synchronize()
+    s64 = sinks.numpy().astype(np.float64)
+    ro1, rl1 = oracle.decode(to_np(q1), Bf16Pool(w["k_cache"]), Bf16Pool(w["v_cache"]),
+                             w["page_table"].numpy(), lens1.numpy(), s64, 0.125)
+    assert_out_close(out1.cpu(), ro1)
+    assert_lse_close(lse1.cpu(), rl1)
+    # the prologue's own outputs at its bar (one bf16 ulp of the float64 reference) ...
+    q2, k2, v2 = qbuf.cpu(), kc.cpu(), vc.cpu()
+    rq, rk, rv = pro.qkv_prologue(to_np(w["qkv"]), to_np(w["bias"]), w["positions"].numpy(),
+                                  np.asarray(inv, dtype=np.float64), ms, hq, hkv)
+    slots = torch.from_numpy(w["slot_mapping"].numpy().astype(np.int64))
+    assert_bf16_close(q2, rq, "q")
+    assert_bf16_close(k2[slots // 16, :, slots % 16], rk, "k")
+    assert_bf16_close(v2[slots // 16, :, slots % 16], rv, "v")
+    # ... and the second decode against the oracle on exactly what it wrote
+    ro2, rl2 = oracle.decode(to_np(q2), Bf16Pool(k2), Bf16Pool(v2), w["page_table"].numpy(),
+                             lens2.numpy(), s64, 0.125)
+    assert_out_close(out2.cpu(), ro2)
+    assert_lse_close(lse2.cpu(), rl2)
