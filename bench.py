@@ -50,7 +50,7 @@ TRAFFIC = {
     "decode": {"sources": ("gqa_attention_learned_gb300/csrc/decode.cu",
                            "gqa_attention_learned_gb300/csrc/kernels.cuh",
                            "gqa_attention_learned_gb300/csrc/ptx.cuh"),
-               "sha256_16": "6bd6fa4ecfea8712", "bytes": 261_729_536 + 3_153_920},
+               "sha256_16": "32c82e9d91842e7b", "bytes": 261_699_328 + 2_998_272},
     "prefill": {"sources": ("gqa_attention_learned_gb300/csrc/prefill.cu",
                             "gqa_attention_learned_gb300/csrc/kernels.cuh",
                             "gqa_attention_learned_gb300/csrc/ptx.cuh"),

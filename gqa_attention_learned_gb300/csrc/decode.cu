@@ -17,6 +17,9 @@
 //    its own STAGES-deep TMA pipeline: lane 0 issues two 3-D bulk tensor
 //    copies per page (K and V tile, 2 KB each, 128-byte swizzle) onto the
 //    stage's mbarrier.  No register staging, so many pages stay in flight.
+//    Pages that only this CTA reads carry an evict-first L2 policy, so the
+//    small tensors every launch re-reads (kv_lens, page table, q) and the
+//    outputs stay in L2.
 //  * The GQA group shares every K/V tile: S^T[16 tok x 8 heads] = K . Q^T and
 //    O^T[64 x 8] += V^T . P^T, each 4 mma.sync.m16n8k16 (bf16 in, fp32 acc).
 //    P^T goes from the score accumulator layout to the B-operand layout with
@@ -29,8 +32,10 @@
 //    finished in place; otherwise each chunk CTA writes (o/d, lse) to the
 //    workspace and bumps the (request, KV head)'s counter, and the last one
 //    to arrive merges the chunks by log-sum-exp -- no second launch.
-// There is no tensor-memory (tcgen05) path here: n = 8 query heads per KV
-// head is far below tcgen05's minimum tile, and the work is bound by HBM.
+// There is no tensor-memory (tcgen05) path here: 8 query heads per KV head
+// would fill 8 rows of a 128-row tcgen05 tile, or (keys as the rows) need
+// 128-key tiles at the tensor pipe's ~46 cycles per instruction, while the
+// work is bound by HBM and mma.sync keeps pace with it.
 
 #include "kernels.cuh"
 #include "ptx.cuh"
