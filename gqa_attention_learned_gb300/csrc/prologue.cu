@@ -19,6 +19,9 @@
 // (token, head row, dims 8c..8c+7 and 8c+32..8c+39) item: two coalesced
 // 16-byte loads, the bias added in fp32, the rotation in fp32, one rounding
 // to bf16, and 16-byte stores to q_out or to the token's cache slot.
+// Launched programmatically: it waits for the previous kernel on the stream
+// before any memory access and lets the next one (the decode of the layer)
+// start ranking its requests at once.
 
 #include "kernels.cuh"
 #include "ptx.cuh"
