@@ -54,7 +54,7 @@ TRAFFIC = {
     "prefill": {"sources": ("gqa_attention_learned_gb300/csrc/prefill.cu",
                             "gqa_attention_learned_gb300/csrc/kernels.cuh",
                             "gqa_attention_learned_gb300/csrc/ptx.cuh"),
-                "sha256_16": "f39f01e674f405cb", "bytes": 223_187_200 + 139_803_904},
+                "sha256_16": "5c75eae3ef74e629", "bytes": 222_833_920 + 139_865_856},
 }
 
 
@@ -652,6 +652,9 @@ def verify_kernel(batch, q_len, hq, hkv, max_kv_len, num_sms=152):
     tiles = -(-q_len // max(1, 128 // g)) if 128 % g == 0 else 0
     if (q_len >= 2 and 128 % g == 0 and q_len * g >= 24 and -(-max_kv_len // 16) <= 512
             and tiles * batch * hkv >= 2 * num_sms):
+        if q_len * g <= 64:               # every key tile split between two softmax warps
+            return ("prefill_kernel<true, true, true> (tcgen05, key halves; rows = tokens x heads "
+                    "of a KV head)")
         return "prefill_kernel<true, true> (tcgen05; rows = tokens x heads of a KV head)"
     nb = 2 if q_len * g > 8 else 1
     return f"decode_kernel<{nb}, true> (mma.sync; rows = tokens x heads of a KV head)"

@@ -361,15 +361,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
   const int key_end = shift + i0 + rows_tok;               // keys needed, exclusive (<= kv_len)
   const int n_tiles = cdiv(key_end, kBN);
   const int npages = cdiv(kv_len, kPageSize);
-  // Verification with 33 to 64 query rows (kHalf) splits every key tile in two:
+  // Verification with up to 64 query rows (kHalf) splits every key tile in two:
   // the rows are replicated into the next tensor-memory lanes (half_rows
   // further on), the warps on the original rows take keys 0..63 of each
   // tile and those on the replica keys 64..127, each half with its own
   // online softmax (the sink counted in the first half only); the halves
   // merge by log-sum-exp at the end.  Each softmax warp then does half the
-  // exponentials of a tile (8-node draft tree, 64 rows: 4797 -> 5140 GB/s).
-  // With 32 rows or fewer, one warp's rows measured faster unsplit (4 draft
-  // tokens: 5467 vs 5349 GB/s).
+  // exponentials of a tile (8-node draft tree, 64 rows: 4797 -> 5140 GB/s;
+  // 4 draft tokens, 32 rows: 5604 -> 5670 GB/s).
   const int half_rows = 32 * cdiv(rows, 32);
   constexpr bool half_keys = kHalf;           // chosen by the host from q_len * group
   // softmax threads with a query row (verification tiles may be partly empty)
@@ -741,7 +740,7 @@ cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap,
   if (p.verify) {
     // one query tile per KV head when verifying (q_len * group <= 128 rows)
     const int rows = p.max_q_len * p.group;
-    if (SA_VERIFY_HALF_KEYS && rows > 32 && rows <= 64)
+    if (SA_VERIFY_HALF_KEYS && rows <= 64)
       return launch_prefill_variant<true, true, true>(qmap, kmap, vmap, p, static_cast<unsigned>(ctas), stream, programmatic);
     return launch_prefill_variant<true, true>(qmap, kmap, vmap, p, static_cast<unsigned>(ctas), stream, programmatic);
   }
